@@ -1,0 +1,11 @@
+"""GB300-native fused attention forward for attention variants.
+
+The computation lives in the CUDA library ``libflattn.so`` (C ABI in
+``include/flattn.h``); this package holds the build step, a thin ctypes
+binding with the same entry-point names, the FLOP/byte accounting used for
+the roofline, and the seeded synthetic-input generators.
+"""
+from .api import (FlattnError, attn_fwd, diffattn_fwd, evoformer_gated_attn_fwd,  # noqa: F401
+                  sync_status)
+
+__all__ = ["attn_fwd", "diffattn_fwd", "evoformer_gated_attn_fwd", "sync_status", "FlattnError"]

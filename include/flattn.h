@@ -1,0 +1,171 @@
+/*
+ * flattn -- fused attention forward for attention variants, sm_103a (GB300).
+ *
+ * One pass computes   out = softmax(score_mod(scale * Q K^T) + mask/bias) V
+ * with an online softmax, the way the Flashlight pages describe the fused
+ * kernel their compiler emits:
+ *   - Flashlight technical summary (gist.science), Methodology, "Structural
+ *     Fusion with Dimension Demotion" (QK^T fused with the row max),
+ *     "Semantic Fusion with Algebraic Transformation" (online softmax with a
+ *     running max and sum, rescaled by e^(x-y) = e^x / e^y), "Tiling-Aware
+ *     Dimension Elimination and Logical Grids" (contiguous tiles, softmax(QK^T)V
+ *     in one kernel); Key Contributions, "Kernel-Level Fusion".
+ *   - Variant list: Flashlight wiki summary (papers.lqhl.me), 实验与结果
+ *     (Vanilla, ALiBi, Softcap, Causal, Sliding Window, PrefixLM, Document
+ *     Mask; MHA/GQA), and 问题与动机 / Results (differential attention,
+ *     Evoformer row-wise gated self-attention).  The pages give no formula for
+ *     any variant; the definitions below are this library's readings.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are bf16 (q, k, v, gate, out) or fp32 (biases, lse), live in
+ *     device memory owned by the caller, and have the head dimension
+ *     contiguous.  Pointers and every non-unit stride (in bytes) must be
+ *     multiples of 16 bytes (the TMA rule); otherwise FL_ERR_ALIGNMENT.
+ *   - Calls are asynchronous on the given stream (NULL = legacy default
+ *     stream).  Argument errors are returned before anything is launched.
+ *   - Errors detected on the device (a pipeline wait that exceeded its time
+ *     limit) are recorded in a per-device status word; fl_sync_status()
+ *     synchronises the stream and returns and clears it.
+ *   - The library allocates, once per device and on the first call that
+ *     needs it, a small status word; it allocates nothing else.
+ *   - lse (log-sum-exp of the final scores, natural log, fp32) may be NULL.
+ *   - Query rows with no visible key produce out = 0 and lse = -inf.
+ */
+#ifndef FLATTN_H_
+#define FLATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FL_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FL_API __attribute__((visibility("default")))
+#else
+#define FL_API
+#endif
+
+typedef enum {
+  FL_OK = 0,
+  FL_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad variant field      */
+  FL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head dim 96)    */
+  FL_ERR_ALIGNMENT = 3,     /* pointer or stride not 16-byte aligned           */
+  FL_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed             */
+  FL_ERR_TIMEOUT = 5,       /* a device-side pipeline wait hit its time limit  */
+  FL_ERR_DEVICE_BOUNDS = 6  /* reserved: a device-side bounds check tripped    */
+} fl_status;
+
+typedef enum {
+  FL_MASK_NONE = 0,           /* every key visible                              */
+  FL_MASK_CAUSAL = 1,         /* key j visible to query i iff j <= i            */
+  FL_MASK_SLIDING_WINDOW = 2, /* iff i - window < j <= i (window keys, self incl.) */
+  FL_MASK_PREFIX_LM = 3,      /* iff j <= i or j < prefix_len                   */
+  FL_MASK_DOCUMENT = 4        /* iff doc(i) == doc(j) [and j <= i if doc_causal] */
+} fl_mask_kind;
+
+typedef enum {
+  FL_SCORE_NONE = 0,    /* t = s                                   */
+  FL_SCORE_ALIBI = 1,   /* t = s + alibi_slopes[h] * (j - i)       */
+  FL_SCORE_SOFTCAP = 2  /* t = softcap * tanh(s / softcap)         */
+} fl_score_mod;
+
+/* Debug switches (fl_attn_desc.debug_flags). */
+#define FL_DEBUG_SKIP_KV_LOAD 0x1u /* block 0 never loads key tile `debug_arg`
+                                      of its first work unit: its pipeline
+                                      wait runs out and the call reports
+                                      FL_ERR_TIMEOUT (tests the bounded waits) */
+
+/*
+ * Problem descriptor for fl_attn_fwd / fl_diffattn_fwd.
+ *   q   [B, Hq,  Lq, d]     k [B, Hkv, Lk, d]     v [B, Hkv, Lk, dv]
+ *   out [B, Hq,  Lq, dv]    lse [B, Hq, Lq] (contiguous)
+ * Strides are in elements, ordered (b, h, l, c); the c stride is 1.  A
+ * zero stride array means contiguous.  s = scale * q.k (scale <= 0 selects
+ * 1/sqrt(d)); GQA maps query head h to key/value head h / (Hq / Hkv).
+ */
+typedef struct fl_attn_desc {
+  int32_t B, Hq, Hkv, Lq, Lk, d, dv;
+  float scale;
+  int32_t mask_kind;        /* fl_mask_kind; masks other than NONE need Lq == Lk */
+  int32_t doc_causal;       /* DOCUMENT only: also require j <= i              */
+  int32_t window;           /* SLIDING_WINDOW: >= 1                            */
+  int32_t prefix_len;       /* PREFIX_LM: >= 0                                 */
+  int32_t score_mod;        /* fl_score_mod                                    */
+  float softcap;            /* SOFTCAP: > 0                                    */
+  const float* alibi_slopes;   /* ALIBI: device fp32 [Hq]                      */
+  const int32_t* doc_offsets;  /* DOCUMENT: device int32 [B, num_docs + 1],
+                                  offsets[b][0] = 0, strictly increasing,
+                                  offsets[b][num_docs] = Lq                    */
+  int32_t num_docs;
+  int64_t q_strides[4], k_strides[4], v_strides[4], o_strides[4];
+  void* stream;             /* cudaStream_t                                    */
+  uint32_t debug_flags;     /* FL_DEBUG_*; 0 in normal use                     */
+  int32_t debug_arg;
+  uint32_t wait_limit_ms;   /* device wait limit; 0 = default (2000 ms)        */
+  int32_t reserved[7];
+} fl_attn_desc;
+
+/* Fill *desc with zeros and the defaults (mask NONE, score NONE, scale 1/sqrt(d)). */
+FL_API void fl_attn_desc_init(fl_attn_desc* desc);
+
+/*
+ * Fused attention forward, variants V1-V8: vanilla MHA, GQA, ALiBi, tanh
+ * softcap, causal, sliding window, prefix-LM, document mask (score_mod and
+ * mask compose).  Supported: d in {32, 64, 128}, dv == d, Hq % Hkv == 0,
+ * any Lq, Lk >= 1 (ragged tails are masked inside the kernel).  Fully masked
+ * key tiles are skipped from the descriptor alone (no block mask is built).
+ */
+FL_API fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      const fl_attn_desc* desc);
+
+/*
+ * Differential attention (the Flashlight pages, Problem Statement and Results,
+ * name it; definition is this library's reading):
+ *   out = softmax(scale Q1 K1^T) V - lambda * softmax(scale Q2 K2^T) V
+ * q1, k1, q2, k2 [B, H, L, d] (d = 64), v [B, H, L, dv] (dv = 128),
+ * out [B, H, L, dv]; lse (may be NULL) is [2, B, H, L]: branch 1 then branch 2.
+ * desc: Hq == Hkv == H, Lq == Lk == L, d, dv, scale, mask_kind NONE or CAUSAL;
+ * strides must be zero (contiguous).  lambda must be finite.
+ */
+FL_API fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                          const void* v, void* out, float* lse, float lambda,
+                          const fl_attn_desc* desc);
+
+/*
+ * AlphaFold Evoformer MSA row-wise gated self-attention (the Flashlight wiki
+ * summary, 设计取舍, notes its extra broadcast bias dimension):
+ *   t[i,j] = scale q_i.k_j + pair_bias[b,h,i,j] + mask_bias[b,s,j]
+ *   out    = sigmoid(gate) * softmax_j(t) V
+ * q, k, v, gate, out : bf16 [B, N_seq, H, N_res, d] contiguous, d in {32, 64}
+ * pair_bias          : fp32 [B, H, N_res, N_res] (shared by all N_seq rows), or NULL
+ * mask_bias          : fp32 [B, N_seq, N_res] (e.g. 0 / -1e9), or NULL
+ * lse                : fp32 [B, N_seq, H, N_res], or NULL
+ * scale <= 0 selects 1/sqrt(d).
+ */
+FL_API fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* v,
+                                      const float* pair_bias, const float* mask_bias,
+                                      const void* gate, void* out, float* lse, int32_t B,
+                                      int32_t N_seq, int32_t N_res, int32_t H, int32_t d,
+                                      float scale, void* stream);
+
+/* Synchronise `stream`, then return and clear the device status word of the
+   current device (FL_OK, or FL_ERR_TIMEOUT if a kernel gave up waiting). */
+FL_API fl_status fl_sync_status(void* stream);
+
+/* Static description of a status code. */
+FL_API const char* fl_status_string(fl_status status);
+
+/* FL_ABI_VERSION of the loaded library. */
+FL_API int32_t fl_abi_version(void);
+
+/* sizeof(fl_attn_desc) as compiled into the library (binding layout check). */
+FL_API int32_t fl_attn_desc_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLATTN_H_ */

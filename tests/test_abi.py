@@ -1,0 +1,135 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/flattn.h declares, agrees with the binding on the descriptor layout,
+and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from flashattention_attn_fwd_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_lib.LIB_PATH):
+        from flashattention_attn_fwd_gb300.build import build
+        build()
+    return _lib.lib()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"FL_API\s+[\w\s\*]+?\b(fl_\w+)\s*\(", txt)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert L.fl_abi_version() == 1
+    assert L.fl_attn_desc_size() == ctypes.sizeof(_lib.AttnDesc)
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = _lib.status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+
+
+def _desc(**kw):
+    d = _lib.new_desc()
+    base = dict(B=1, Hq=2, Hkv=2, Lq=128, Lk=128, d=64, dv=64)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+P = 0x10000  # a 16-byte aligned fake device address; never dereferenced
+
+
+def _attn(L, desc, q=P, k=P, v=P, o=P, lse=0):
+    return L.fl_attn_fwd(q, k, v, o, lse, ctypes.byref(desc))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=0), _lib.FL_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), _lib.FL_ERR_INVALID_ARG),
+    (dict(Lq=0), _lib.FL_ERR_INVALID_ARG),
+    (dict(d=96, dv=96), _lib.FL_ERR_UNSUPPORTED),
+    (dict(dv=32), _lib.FL_ERR_UNSUPPORTED),
+    (dict(mask_kind=9), _lib.FL_ERR_INVALID_ARG),
+    (dict(mask_kind=1, Lk=64), _lib.FL_ERR_UNSUPPORTED),
+    (dict(mask_kind=2, window=0), _lib.FL_ERR_INVALID_ARG),
+    (dict(mask_kind=3, prefix_len=-1), _lib.FL_ERR_INVALID_ARG),
+    (dict(mask_kind=4, num_docs=2), _lib.FL_ERR_INVALID_ARG),       # no offsets
+    (dict(score_mod=1), _lib.FL_ERR_INVALID_ARG),                   # no slopes
+    (dict(score_mod=2, softcap=0.0), _lib.FL_ERR_INVALID_ARG),
+    (dict(score_mod=2, softcap=float("inf")), _lib.FL_ERR_INVALID_ARG),
+    (dict(score_mod=7), _lib.FL_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.FL_ERR_INVALID_ARG),
+])
+def test_attn_rejects_bad_descriptor(L, kw, expect):
+    assert _attn(L, _desc(**kw)) == expect
+
+
+def test_attn_rejects_null_and_misaligned(L):
+    d = _desc()
+    assert _attn(L, d, q=0) == _lib.FL_ERR_INVALID_ARG
+    assert _attn(L, d, o=0) == _lib.FL_ERR_INVALID_ARG
+    assert L.fl_attn_fwd(P, P, P, P, 0, None) == _lib.FL_ERR_INVALID_ARG
+    assert _attn(L, d, k=P + 8) == _lib.FL_ERR_ALIGNMENT
+    assert _attn(L, d, lse=P + 2) == _lib.FL_ERR_ALIGNMENT
+    d2 = _desc()
+    d2.q_strides = (ctypes.c_int64 * 4)(2 * 128 * 68, 128 * 68, 68, 1)  # row stride 136 bytes
+    assert _attn(L, d2) == _lib.FL_ERR_ALIGNMENT
+    d3 = _desc()
+    d3.q_strides = (ctypes.c_int64 * 4)(1, 1, 64, 2)  # channel stride must be 1
+    assert _attn(L, d3) == _lib.FL_ERR_INVALID_ARG
+
+
+def test_diffattn_rejects(L):
+    d = _desc(d=64, dv=128)
+    f = L.fl_diffattn_fwd
+    assert f(P, P, P, P, P, P, 0, ctypes.c_float(float("nan")), ctypes.byref(d)) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, 0, P, P, P, P, 0, ctypes.c_float(0.8), ctypes.byref(d)) == _lib.FL_ERR_INVALID_ARG
+    bad = _desc(d=64, dv=64)
+    assert f(P, P, P, P, P, P, 0, ctypes.c_float(0.8), ctypes.byref(bad)) == _lib.FL_ERR_UNSUPPORTED
+    win = _desc(d=64, dv=128, mask_kind=2, window=4)
+    assert f(P, P, P, P, P, P, 0, ctypes.c_float(0.8), ctypes.byref(win)) == _lib.FL_ERR_UNSUPPORTED
+    gqa = _desc(d=64, dv=128, Hq=4, Hkv=2)
+    assert f(P, P, P, P, P, P, 0, ctypes.c_float(0.8), ctypes.byref(gqa)) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P, P, P + 4, P, 0, ctypes.c_float(0.8), ctypes.byref(d)) == _lib.FL_ERR_ALIGNMENT
+
+
+def test_evoformer_rejects(L):
+    f = L.fl_evoformer_gated_attn_fwd
+    s = ctypes.c_float(0.0)
+    assert f(P, P, P, P, P, 0, P, 0, 1, 4, 256, 8, 32, s, None) == _lib.FL_ERR_INVALID_ARG  # no gate
+    assert f(P, P, P, P, P, P, P, 0, 1, 4, 256, 8, 48, s, None) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, 0, 0, 4, 256, 8, 32, s, None) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P, P + 4, P, P, P, 0, 1, 4, 256, 8, 32, s, None) == _lib.FL_ERR_ALIGNMENT
+    assert f(P, P, P, P, P, P, P, 0, 1, 4, 250, 8, 32, s, None) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, 0, 1, 4, 256, 8, 32, ctypes.c_float(float("inf")), None) == _lib.FL_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    assert _attn(L, _desc()) == _lib.FL_ERR_CUDA
+    assert L.fl_sync_status(None) == _lib.FL_ERR_CUDA
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    from flashattention_attn_fwd_gb300 import attn_fwd
+    q = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn_fwd(q, q, q)
