@@ -34,6 +34,7 @@ EXPORTS = (
     "fl_status_string",
     "fl_abi_version",
     "fl_attn_desc_size",
+    "fl_attn_fwd_noalloc",
 )
 
 
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.fl_attn_desc_init.restype = None
         L.fl_attn_fwd.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(AttnDesc)]
         L.fl_attn_fwd.restype = i32
+        L.fl_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(AttnDesc)]
+        L.fl_attn_fwd_noalloc.restype = i32
         L.fl_diffattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, ctypes.POINTER(AttnDesc)]
         L.fl_diffattn_fwd.restype = i32
         L.fl_evoformer_gated_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]

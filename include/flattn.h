@@ -151,6 +151,33 @@ FL_API fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const
                                       int32_t N_seq, int32_t N_res, int32_t H, int32_t d,
                                       float scale, void* stream);
 
+/*
+ * Allocation-free variant of fl_attn_fwd (no counterpart in the paper; it is
+ * a property of this library's interface).  For callers that cannot let a
+ * library call cudaMalloc: processes whose device memory all comes from
+ * their own pre-reserved pool or arena, code that must not allocate while a
+ * stream is captured into a CUDA graph, and callers with a hard memory
+ * budget.  Same arguments, results and errors as fl_attn_fwd, but the
+ * kernel's status words live in a 256-byte array compiled into the library
+ * (present on every GPU that loads it, until the process exits) instead of
+ * a cudaMalloc'd word, and nothing is allocated.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream
+ *     capture.
+ *   - The scratch needed per call is 8 bytes whatever the problem size; a
+ *     requirement above the array's 256 bytes would return
+ *     FL_ERR_UNSUPPORTED.
+ *   - All calls on a device share the array and it keeps what the last call
+ *     wrote: a device-side timeout stays recorded until queried.  Calls that
+ *     overlap on the GPU (different streams) race on it: a failure is
+ *     reported to whichever query comes next.
+ *   - Query mode: with q, k, v, out and lse all NULL the call synchronises
+ *     desc->stream and returns (and clears) the recorded status: FL_OK or
+ *     FL_ERR_TIMEOUT.  fl_sync_status does not see this path's status.
+ */
+FL_API fl_status fl_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                                     const fl_attn_desc* desc);
+
 /* Synchronise `stream`, then return and clear the device status word of the
    current device (FL_OK, or FL_ERR_TIMEOUT if a kernel gave up waiting). */
 FL_API fl_status fl_sync_status(void* stream);
