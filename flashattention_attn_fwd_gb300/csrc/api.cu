@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -203,6 +204,10 @@ fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   p.status = ds->status;
   p.timeout_ns = wait_ns(d.wait_limit_ms);
   p.dbg_skip_tile = (d.debug_flags & FL_DEBUG_SKIP_KV_LOAD) ? (d.debug_arg < 0 ? 0 : d.debug_arg) : -1;
+#ifdef FL_TRACE
+  if (const char* tp = std::getenv("FLATTN_TRACE_PTR"))
+    p.trace = reinterpret_cast<unsigned long long*>(std::strtoull(tp, nullptr, 0));
+#endif
   int64_t units;
   if (p.group == 1) {
     p.slot_mode = fl::SLOT_ROWS;
@@ -215,11 +220,12 @@ fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[5];
+  CUtensorMap maps[6];
   const int bq = box_width(d.d), bv = box_width(d.dv);
   if (!encode_bhlc(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sq.l, sq.h, sq.b, bq) ||
       !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sk.l, sk.h, sk.b, bq) ||
-      !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bv))
+      !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bv) ||
+      !encode_bhlc(&maps[5], out, d.dv, d.Lq, d.Hq, d.B, so.l, so.h, so.b, bv))
     return FL_ERR_CUDA;
   maps[3] = maps[0];
   maps[4] = maps[1];
@@ -272,14 +278,16 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
   if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[5];
+  CUtensorMap maps[6];
   const int64_t sl = 64, sh = static_cast<int64_t>(L) * 64, sb = static_cast<int64_t>(H) * L * 64;
   if (!encode_bhlc(&maps[0], q1, 64, L, H, d.B, sl, sh, sb, 64) ||
       !encode_bhlc(&maps[1], k1, 64, L, H, d.B, sl, sh, sb, 64) ||
       !encode_bhlc(&maps[2], v, 128, L, H, d.B, 128, static_cast<int64_t>(L) * 128,
                    static_cast<int64_t>(H) * L * 128, 64) ||
       !encode_bhlc(&maps[3], q2, 64, L, H, d.B, sl, sh, sb, 64) ||
-      !encode_bhlc(&maps[4], k2, 64, L, H, d.B, sl, sh, sb, 64))
+      !encode_bhlc(&maps[4], k2, 64, L, H, d.B, sl, sh, sb, 64) ||
+      !encode_bhlc(&maps[5], out, 128, L, H, d.B, 128, static_cast<int64_t>(L) * 128,
+                   static_cast<int64_t>(H) * L * 128, 64))
     return FL_ERR_CUDA;
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
   cudaError_t e = fl::launch_diff_d64(maps, p, grid, static_cast<cudaStream_t>(d.stream));
@@ -321,12 +329,13 @@ fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* 
   if (units > 0x7fffffff || Bf > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[5];
+  CUtensorMap maps[6];
   const int bw = box_width(d);
   const int64_t sl = d, sh = static_cast<int64_t>(N_res) * d, sb = static_cast<int64_t>(H) * N_res * d;
   if (!encode_bhlc(&maps[0], q, d, N_res, H, Bf, sl, sh, sb, bw) ||
       !encode_bhlc(&maps[1], k, d, N_res, H, Bf, sl, sh, sb, bw) ||
-      !encode_bhlc(&maps[2], v, d, N_res, H, Bf, sl, sh, sb, bw))
+      !encode_bhlc(&maps[2], v, d, N_res, H, Bf, sl, sh, sb, bw) ||
+      !encode_bhlc(&maps[5], out, d, N_res, H, Bf, sl, sh, sb, bw))
     return FL_ERR_CUDA;
   maps[3] = maps[0];
   maps[4] = maps[1];

@@ -206,11 +206,12 @@ fl_status fl_attn_fwd_noalloc(const void* q, const void* k, const void* v, void*
   if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[5];
+  CUtensorMap maps[6];
   const int bq = d.d >= 64 ? 64 : d.d;
   if (!na_map(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sq.l, sq.h, sq.b, bq) ||
       !na_map(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sk.l, sk.h, sk.b, bq) ||
-      !na_map(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bq))
+      !na_map(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bq) ||
+      !na_map(&maps[5], out, d.dv, d.Lq, d.Hq, d.B, so.l, so.h, so.b, bq))
     return FL_ERR_CUDA;
   maps[3] = maps[0];
   maps[4] = maps[1];

@@ -18,7 +18,9 @@ enum SlotMode : int { SLOT_ROWS = 0, SLOT_HEADS = 1, SLOT_BRANCH = 2 };
 
 constexpr int kBlockM = 128;  // query rows per slot (one TMEM lane per row)
 constexpr int kBlockN = 128;  // keys per key/value tile
-constexpr int kThreads = 320; // warp 0: TMA, warp 1: MMA, warps 2-9: softmax (2 x 4)
+// warp 0: TMA; warps 1 and 10: MMA issue for slot 0 / slot 1; warps 2-9:
+// softmax (4 warps per slot)
+constexpr int kThreads = 352;
 
 struct KParams {
   // problem (for the Evoformer, B is B * N_seq and Hq == Hkv == H)
@@ -57,6 +59,8 @@ struct KParams {
   uint32_t* status;         // device status word (bit 0: timeout), [1]: where
   uint64_t timeout_ns;
   int dbg_skip_tile;        // < 0: off
+  // Phase timestamps of block 0 (builds with -DFL_TRACE only): [role 4][tile 64][event 8]
+  unsigned long long* trace;
 };
 
 }  // namespace fl

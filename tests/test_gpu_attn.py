@@ -198,3 +198,15 @@ def test_skipped_tile_load_times_out_then_recovers():
     sync_status()
     ro, rl = oracle.attention(q, k, v)
     check(out, ro, lse, rl)
+
+
+def test_softcap_both_tanh_paths():
+    """Scores inside the polynomial range (|s*scale/cap| <= 0.5) take the FMA
+    path, a large-score tile takes the exact MUFU path; both must match."""
+    q, k, v = synth.attn_inputs(1, 2, 2, 300, 64, seed=41)
+    for cap, qs in ((30.0, 1.0), (2.0, 1.0), (30.0, 40.0)):
+        qq = (q.float() * qs).to(torch.bfloat16)
+        out, lse = attn_fwd(*_gpu(qq, k, v), score_mod="softcap", softcap=cap)
+        sync_status()
+        ro, rl = oracle.attention(qq, k, v, score_mod="softcap", softcap=cap)
+        check(out, ro, lse, rl)
