@@ -21,6 +21,7 @@ __all__ = [
     "doc_offsets",
     "diff_inputs",
     "evo_inputs",
+    "evo_col_inputs",
 ]
 
 
@@ -105,3 +106,28 @@ def evo_inputs(B: int, N_seq: int, N_res: int, H: int, d: int = 32, seed: int = 
     mask_bias = torch.where(keep, torch.zeros((), dtype=torch.float32),
                             torch.full((), mask_value, dtype=torch.float32))
     return q, k, v, pair_bias, mask_bias, gate
+
+
+def evo_col_inputs(B: int, N_seq: int, N_res: int, H: int, d: int = 32, seed: int = 0,
+                   p_keep: float = 0.9, mask_value: float = -1e9):
+    """Evoformer MSA column-attention inputs.
+
+    q, k, v, gate : bf16 [B, N_seq, H, N_res, d], N(0,1) (gate holds logits)
+    mask_bias     : fp32 [B, N_res, N_seq], 0 where the MSA row is kept
+                    (Bernoulli(p_keep)) and ``mask_value`` where it is masked.
+    Every residue column keeps at least one MSA row.
+    """
+    g = generator(seed)
+    q = randn_bf16((B, N_seq, H, N_res, d), g)
+    k = randn_bf16((B, N_seq, H, N_res, d), g)
+    v = randn_bf16((B, N_seq, H, N_res, d), g)
+    gate = randn_bf16((B, N_seq, H, N_res, d), g)
+    keep = torch.rand(B, N_res, N_seq, generator=g) < p_keep
+    empty = ~keep.any(dim=-1)
+    if bool(empty.any()):
+        first = torch.zeros_like(keep)
+        first[..., 0] = True
+        keep = keep | (first & empty[..., None])
+    mask_bias = torch.where(keep, torch.zeros((), dtype=torch.float32),
+                            torch.full((), mask_value, dtype=torch.float32))
+    return q, k, v, mask_bias, gate

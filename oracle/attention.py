@@ -40,6 +40,10 @@ readings taken here are:
 * Differential out = softmax(Q1 K1^T s) V - lambda softmax(Q2 K2^T s) V.
 * Evoformer    t = s + pair_bias[h, i, j] + mask_bias[msa_row, j];
                out = sigmoid(gate) * (P V).
+* Evoformer, column-wise: for each residue column r, attention over the MSA
+               rows s with t = s + mask_bias[r, s'] and no pair bias;
+               out = sigmoid(gate) * (P V) (technical summary, Results, names
+               the row- and column-wise gated forms).
 * A row with no visible key gives O = 0 and LSE = -inf.
 
 All arithmetic is float64 NumPy; a matmul and ``exp``/``log``/``tanh`` are
@@ -62,6 +66,8 @@ __all__ = [
     "diff_attention_rows",
     "evoformer_gated_attention",
     "evoformer_rows",
+    "evoformer_col_gated_attention",
+    "evoformer_col_rows",
 ]
 
 MASKS = ("none", "causal", "window", "prefix_lm", "document")
@@ -296,5 +302,43 @@ def evoformer_rows(q, k, v, pair_bias, mask_bias, gate, rows, *, scale=None):
         t = (scale * (k[b, s, h] @ q[b, s, h, i]) + pb[b, h, i] + mb[b, s])[None, :]
         P, l = softmax_rows(t)
         outs.append(_sigmoid(gate[b, s, h, i]) * (P @ v[b, s, h])[0])
+        lses.append(l[0])
+    return np.array(outs), np.array(lses)
+
+
+def evoformer_col_gated_attention(q, k, v, mask_bias, gate, *, scale: float | None = None):
+    """Evoformer MSA column-wise gated self-attention.
+
+    q, k, v, gate : [B, N_seq, H, N_res, d] (the MSA layout of the row-wise
+    form);  mask_bias : [B, N_res, N_seq] (added to every query of residue
+    column r, per key MSA row).  For every (b, h, r) attention runs over the
+    MSA-row axis.  Returns (out [B,N_seq,H,N_res,d], lse [B,H,N_res,N_seq])."""
+    q, k, v, gate = _f64(q), _f64(k), _f64(v), _f64(gate)
+    mb = _f64(mask_bias)
+    B, Ns, H, Nr, d = q.shape
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    out = np.zeros_like(q)
+    lse = np.zeros((B, H, Nr, Ns))
+    for b in range(B):
+        for h in range(H):
+            for r in range(Nr):
+                t = scale * (q[b, :, h, r] @ k[b, :, h, r].T) + mb[b, r][None, :]
+                P, l = softmax_rows(t)
+                out[b, :, h, r] = _sigmoid(gate[b, :, h, r]) * (P @ v[b, :, h, r])
+                lse[b, h, r] = l
+    return out, lse
+
+
+def evoformer_col_rows(q, k, v, mask_bias, gate, rows, *, scale=None):
+    """Column-wise Evoformer output for a list of (b, msa_row, h, r) query rows."""
+    q, k, v, gate = _f64(q), _f64(k), _f64(v), _f64(gate)
+    mb = _f64(mask_bias)
+    d = q.shape[-1]
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    outs, lses = [], []
+    for (b, s, h, r) in rows:
+        t = (scale * (k[b, :, h, r] @ q[b, s, h, r]) + mb[b, r])[None, :]
+        P, l = softmax_rows(t)
+        outs.append(_sigmoid(gate[b, s, h, r]) * (P @ v[b, :, h, r])[0])
         lses.append(l[0])
     return np.array(outs), np.array(lses)

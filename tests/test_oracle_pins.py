@@ -372,6 +372,70 @@ def test_brute_force_evoformer():
                 assert lse[0, s, h, i] == pytest.approx(l, abs=1e-12)
 
 
+def test_evoformer_col_is_row_form_on_transposed_msa():
+    """Column-wise attention over MSA rows = the (separately pinned) row-wise
+    form on the MSA with its two axes swapped, with zero pair bias and the
+    column mask as the row mask."""
+    B, Ns, H, Nr, d = 2, 7, 2, 5, 4
+    q, k, v, g = (_rand(B, Ns, H, Nr, d) for _ in range(4))
+    mb = np.where(RNG.random((B, Nr, Ns)) < 0.7, 0.0, -1e9)
+    mb[..., 0] = 0.0
+    out, lse = oracle.evoformer_col_gated_attention(q, k, v, mb, g)
+    tr = lambda x: np.ascontiguousarray(np.swapaxes(x, 1, 3))  # noqa: E731
+    ro, rl = oracle.evoformer_gated_attention(tr(q), tr(k), tr(v), np.zeros((B, H, Ns, Ns)), mb, tr(g))
+    np.testing.assert_allclose(out, tr(ro), atol=1e-13)
+    np.testing.assert_allclose(lse, np.swapaxes(rl, 1, 2), atol=1e-13)
+
+
+def test_evoformer_col_closed_forms():
+    """q = 0: every visible MSA row weighs the same, so out is sigmoid(gate)
+    times the mean of the visible V rows of that column and lse = log
+    #visible; a mask keeping one MSA row s0 copies V[s0]."""
+    B, Ns, H, Nr, d = 1, 6, 2, 3, 4
+    k, v, g = (_rand(B, Ns, H, Nr, d) for _ in range(3))
+    q = np.zeros((B, Ns, H, Nr, d))
+    mb = np.zeros((B, Nr, Ns))
+    mb[0, 1, [0, 2, 5]] = -1e9
+    mb[0, 2, :] = -1e9
+    mb[0, 2, 4] = 0.0
+    out, lse = oracle.evoformer_col_gated_attention(q, k, v, mb, g)
+    sig = 1 / (1 + np.exp(-g))
+    for h in range(H):
+        for s in range(Ns):
+            np.testing.assert_allclose(out[0, s, h, 0], sig[0, s, h, 0] * v[0, :, h, 0].mean(0), atol=1e-12)
+            np.testing.assert_allclose(out[0, s, h, 1], sig[0, s, h, 1] * v[0, [1, 3, 4], h, 1].mean(0), atol=1e-12)
+            np.testing.assert_allclose(out[0, s, h, 2], sig[0, s, h, 2] * v[0, 4, h, 2], atol=1e-12)
+    np.testing.assert_allclose(lse[0, :, 0], math.log(Ns), atol=1e-12)
+    np.testing.assert_allclose(lse[0, :, 1], math.log(3), atol=1e-12)
+
+
+def test_brute_force_evoformer_col():
+    B, Ns, H, Nr, d = 1, 7, 2, 3, 4
+    q, k, v, g = (_rand(B, Ns, H, Nr, d) for _ in range(4))
+    mb = np.where(RNG.random((B, Nr, Ns)) < 0.7, 0.0, -1e9)
+    mb[..., 0] = 0.0
+    out, lse = oracle.evoformer_col_gated_attention(q, k, v, mb, g, scale=0.3)
+    for h in range(H):
+        for r in range(Nr):
+            K = [k[0, s, h, r].tolist() for s in range(Ns)]
+            V = [v[0, s, h, r].tolist() for s in range(Ns)]
+            for s in range(Ns):
+                o, l = brute_row(q[0, s, h, r].tolist(), K, V, s, 0.3, bias_row=mb[0, r].tolist())
+                sig = [1 / (1 + math.exp(-x)) for x in g[0, s, h, r]]
+                np.testing.assert_allclose(out[0, s, h, r], [a * b for a, b in zip(sig, o)], atol=1e-12)
+                assert lse[0, h, r, s] == pytest.approx(l, abs=1e-12)
+
+
+def test_evoformer_col_rows_match_full():
+    e = synth.evo_col_inputs(1, 9, 5, 2, d=8, seed=3)
+    out, lse = oracle.evoformer_col_gated_attention(*e)
+    rows = [(0, 0, 0, 0), (0, 8, 1, 4), (0, 3, 1, 2)]
+    ro, rl = oracle.evoformer_col_rows(*e, rows=rows)
+    for n, (b, s, h, r) in enumerate(rows):
+        np.testing.assert_allclose(ro[n], out[b, s, h, r], atol=1e-13)
+        assert rl[n] == pytest.approx(lse[b, h, r, s], abs=1e-13)
+
+
 @pytest.mark.parametrize("kw", VARIANTS[:-1], ids=lambda kw: "-".join(f"{a}" for a in kw.values() if isinstance(a, (str, int, float))) or "vanilla")
 @pytest.mark.parametrize("block", [4, 16])
 def test_online_equals_two_pass(kw, block):
