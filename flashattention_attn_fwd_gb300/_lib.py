@@ -30,6 +30,7 @@ EXPORTS = (
     "fl_attn_fwd",
     "fl_diffattn_fwd",
     "fl_evoformer_gated_attn_fwd",
+    "fl_evoformer_col_gated_attn_fwd",
     "fl_sync_status",
     "fl_status_string",
     "fl_abi_version",
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.fl_diffattn_fwd.restype = i32
         L.fl_evoformer_gated_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
         L.fl_evoformer_gated_attn_fwd.restype = i32
+        L.fl_evoformer_col_gated_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+        L.fl_evoformer_col_gated_attn_fwd.restype = i32
         L.fl_sync_status.argtypes = [vp]
         L.fl_sync_status.restype = i32
         L.fl_status_string.argtypes = [i32]

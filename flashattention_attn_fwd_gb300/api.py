@@ -156,6 +156,35 @@ def evoformer_gated_attn_fwd(q, k, v, pair_bias, mask_bias, gate, *, scale: floa
     return out, lse
 
 
+def evoformer_col_gated_attn_fwd(q, k, v, mask_bias, gate, *, scale: float | None = None,
+                                 out=None, lse=None, return_lse: bool = True, stream=None):
+    """fl_evoformer_col_gated_attn_fwd: q,k,v,gate [B,N_seq,H,N_res,d] bf16,
+    mask_bias [B,N_res,N_seq] fp32 (or None).  Attention over the MSA rows of
+    every residue column.  Returns (out like q, lse [B,H,N_res,N_seq] fp32 or
+    None)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("gate", gate)):
+        _need(t, name, 5)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Ns, H, Nr, d = q.shape
+    if mask_bias is not None:
+        _need(mask_bias, "mask_bias", 3, torch.float32)
+        if not mask_bias.is_contiguous() or tuple(mask_bias.shape) != (B, Nr, Ns):
+            raise ValueError("mask_bias must be contiguous [B,N_res,N_seq]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 5)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nr, Ns), device=q.device, dtype=torch.float32)
+    st = _lib.lib().fl_evoformer_col_gated_attn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(),
+        0 if mask_bias is None else mask_bias.data_ptr(),
+        gate.data_ptr(), out.data_ptr(), 0 if lse is None else lse.data_ptr(),
+        B, Ns, Nr, H, d, ctypes.c_float(0.0 if scale is None else float(scale)), _stream_ptr(stream))
+    _lib.check(st, "fl_evoformer_col_gated_attn_fwd")
+    return out, lse
+
+
 def sync_status(stream=None) -> int:
     """fl_sync_status: synchronise the stream and return (and clear) the
     device status word; raises FlattnError if a kernel reported a failure."""

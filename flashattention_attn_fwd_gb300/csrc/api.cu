@@ -5,11 +5,11 @@
 
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "flattn.h"
+#include "host.h"
 #include "kernels.h"
 #include "params.h"
 
@@ -19,6 +19,13 @@ using fl::KParams;
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitNs = 2000ull * 1000ull * 1000ull;
+constexpr double kLog2e = 1.4426950408889634;
+
+// tanh(y) ~= y * (p0 + p1 y^2 + p2 y^4 + p3 y^6) for |y| <= kTanhRange, the
+// minimax fit printed by csrc/fit_poly.py (defaults: float32 max relative
+// error 6.2e-7).  The softcap kernels fold scale and cap into these.
+constexpr double kTanhRange = 0.5;
+constexpr float kTanhP[4] = {0.999999464f, -0.333263218f, 0.13190335f, -0.0444031134f};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -69,26 +76,58 @@ fl_status device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Tiled tensor map over `rank` dimensions (innermost first; strides in bytes
+// for dimensions 1..rank-1), box `box`, the given swizzle.
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+            const uint64_t* stride_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1u;
+    if (i + 1 < rank) s[i] = stride_bytes[i];
+  }
+  return enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // 4-D bf16 tensor map over a [B, H, L, C] view (strides in elements; channel
 // stride 1), boxes of box_c channels x 128 rows; swizzle = box_c * 2 bytes.
 bool encode_bhlc(CUtensorMap* m, const void* base, int64_t C, int64_t L, int64_t H, int64_t B, int64_t sl,
                  int64_t sh, int64_t sb, int box_c) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sl * 2), static_cast<cuuint64_t>(sh * 2),
-                           static_cast<cuuint64_t>(sb * 2)};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_c), 128u, 1u, 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUtensorMapSwizzle sw = box_c * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                          : box_c * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_32B;
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const uint64_t dims[4] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(H),
+                            static_cast<uint64_t>(B)};
+  const uint64_t str[3] = {static_cast<uint64_t>(sl * 2), static_cast<uint64_t>(sh * 2),
+                           static_cast<uint64_t>(sb * 2)};
+  const uint32_t box[4] = {static_cast<uint32_t>(box_c), 128u, 1u, 1u};
+  const CUtensorMapSwizzle sw = box_c * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_c * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, str, box, sw);
+}
+
+// fp32 pair bias [B, H, N, N]: boxes of 32 columns x 128 rows, 128-byte swizzle.
+bool encode_pair_bias(CUtensorMap* m, const float* pb, int64_t B, int64_t H, int64_t N) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(N), static_cast<uint64_t>(N), static_cast<uint64_t>(H),
+                            static_cast<uint64_t>(B)};
+  const uint64_t str[3] = {static_cast<uint64_t>(N * 4), static_cast<uint64_t>(N * N * 4),
+                           static_cast<uint64_t>(H * N * N * 4)};
+  const uint32_t box[4] = {32u, 128u, 1u, 1u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// fp32 row-major matrix [rows, cols]: boxes of one 128-column row segment.
+bool encode_rows_f32(CUtensorMap* m, const float* base, int64_t rows, int64_t cols) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t str[1] = {static_cast<uint64_t>(cols * 4)};
+  const uint32_t box[2] = {128u, 1u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 struct Strides {
@@ -116,7 +155,122 @@ int box_width(int c) { return c >= 64 ? 64 : c; }
 
 uint64_t wait_ns(uint32_t ms) { return ms ? static_cast<uint64_t>(ms) * 1000ull * 1000ull : kDefaultWaitNs; }
 
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+// Softcap on the FMA pipe: cap*log2(e)*tanh(s*scale/cap) = s * Q(s^2) while
+// |s * scale / cap| <= kTanhRange (the kernel checks the range per warp).
+void softcap_coefficients(KParams& p, float scale, float cap) {
+  const double ya = static_cast<double>(scale) / cap, k = static_cast<double>(cap) * kLog2e;
+  double ypow = ya;
+  for (int i = 0; i < 4; ++i) {
+    p.sc_q[i] = static_cast<float>(k * kTanhP[i] * ypow);
+    ypow *= ya * ya;
+  }
+  p.sc_smax = static_cast<float>(kTanhRange / ya);
+}
+
+cudaError_t launch_attn(int d, int dv, int score_mod, const CUtensorMap* maps, const KParams& p, int grid,
+                        cudaStream_t s) {
+#define FL_CASE(D, DV) \
+  if (d == D && dv == DV) return fl::launch_attn_d##D##_dv##DV(score_mod, maps, p, grid, s);
+  FL_CASE(32, 32) FL_CASE(32, 64) FL_CASE(32, 128)
+  FL_CASE(64, 32) FL_CASE(64, 64) FL_CASE(64, 128)
+  FL_CASE(128, 32) FL_CASE(128, 64) FL_CASE(128, 128)
+#undef FL_CASE
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+namespace fl {
+
+fl_status attn_fwd_check(const void* q, const void* k, const void* v, void* out, float* lse,
+                         const fl_attn_desc* desc) {
+  if (!desc || !q || !k || !v || !out) return FL_ERR_INVALID_ARG;
+  const fl_attn_desc& d = *desc;
+  if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0) return FL_ERR_INVALID_ARG;
+  if (!head_dim_ok(d.d) || !head_dim_ok(d.dv)) return FL_ERR_UNSUPPORTED;
+  if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind < FL_MASK_NONE || d.mask_kind > FL_MASK_DOCUMENT) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind != FL_MASK_NONE && d.Lq != d.Lk) return FL_ERR_UNSUPPORTED;
+  if (d.mask_kind == FL_MASK_SLIDING_WINDOW && d.window < 1) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind == FL_MASK_PREFIX_LM && d.prefix_len < 0) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind == FL_MASK_DOCUMENT && (!d.doc_offsets || d.num_docs < 1 || d.num_docs > d.Lq))
+    return FL_ERR_INVALID_ARG;
+  if (d.score_mod < FL_SCORE_NONE || d.score_mod > FL_SCORE_SOFTCAP) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_ALIBI && !d.alibi_slopes) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_SOFTCAP && !(d.softcap > 0.f && std::isfinite(d.softcap))) return FL_ERR_INVALID_ARG;
+  Strides sq, sk, sv, so;
+  if (!resolve_strides(d.q_strides, d.Hq, d.Lq, d.d, &sq) || !resolve_strides(d.k_strides, d.Hkv, d.Lk, d.d, &sk) ||
+      !resolve_strides(d.v_strides, d.Hkv, d.Lk, d.dv, &sv) || !resolve_strides(d.o_strides, d.Hq, d.Lq, d.dv, &so))
+    return FL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !strides_aligned(sq) ||
+      !strides_aligned(sk) || !strides_aligned(sv) || !strides_aligned(so))
+    return FL_ERR_ALIGNMENT;
+  if (d.mask_kind == FL_MASK_DOCUMENT && !aligned4(d.doc_offsets)) return FL_ERR_ALIGNMENT;
+  if (lse && !aligned4(lse)) return FL_ERR_ALIGNMENT;
+  return FL_OK;
+}
+
+fl_status attn_fwd_launch(const void* q, const void* k, const void* v, void* out, float* lse,
+                          const fl_attn_desc* desc, uint32_t* status, int sm_count) {
+  const fl_status chk = attn_fwd_check(q, k, v, out, lse, desc);
+  if (chk != FL_OK) return chk;
+  const fl_attn_desc& d = *desc;
+  Strides sq, sk, sv, so;
+  resolve_strides(d.q_strides, d.Hq, d.Lq, d.d, &sq);
+  resolve_strides(d.k_strides, d.Hkv, d.Lk, d.d, &sk);
+  resolve_strides(d.v_strides, d.Hkv, d.Lk, d.dv, &sv);
+  resolve_strides(d.o_strides, d.Hq, d.Lq, d.dv, &so);
+
+  KParams p{};
+  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.Lq = d.Lq; p.Lk = d.Lk;
+  p.group = d.Hq / d.Hkv;
+  p.n_qtiles = (d.Lq + fl::kBlockM - 1) / fl::kBlockM;
+  const float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
+  p.scale = scale;
+  p.scale_log2 = scale * static_cast<float>(kLog2e);
+  p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
+  p.window = d.window; p.prefix = d.prefix_len;
+  p.doc_offsets = d.doc_offsets; p.num_docs = d.num_docs;
+  p.slopes = d.alibi_slopes; p.softcap = d.softcap;
+  if (d.score_mod == FL_SCORE_SOFTCAP) softcap_coefficients(p, scale, d.softcap);
+  p.out = out; p.o_sb = so.b; p.o_sh = so.h; p.o_sl = so.l;
+  p.lse = lse;
+  p.status = status;
+  p.timeout_ns = wait_ns(d.wait_limit_ms);
+  p.dbg_skip_tile = (d.debug_flags & FL_DEBUG_SKIP_KV_LOAD) ? (d.debug_arg < 0 ? 0 : d.debug_arg) : -1;
+  int64_t units;
+  if (p.group == 1) {
+    p.slot_mode = fl::SLOT_ROWS;
+    units = static_cast<int64_t>(d.B) * d.Hq * ((p.n_qtiles + 1) / 2);
+  } else {
+    p.slot_mode = fl::SLOT_HEADS;
+    p.pairs_per_group = (p.group + 1) / 2;
+    units = static_cast<int64_t>(d.B) * d.Hkv * p.pairs_per_group * p.n_qtiles;
+  }
+  if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+
+  CUtensorMap maps[8];
+  const int bq = box_width(d.d), bv = box_width(d.dv);
+  if (!encode_bhlc(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sq.l, sq.h, sq.b, bq) ||
+      !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sk.l, sk.h, sk.b, bq) ||
+      !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bv) ||
+      !encode_bhlc(&maps[5], out, d.dv, d.Lq, d.Hq, d.B, so.l, so.h, so.b, bv))
+    return FL_ERR_CUDA;
+  maps[3] = maps[0];
+  maps[4] = maps[1];
+  maps[6] = maps[0];
+  maps[7] = maps[0];
+
+  const int grid = static_cast<int>(units < sm_count ? units : sm_count);
+  const cudaError_t e =
+      launch_attn(d.d, d.dv, d.score_mod, maps, p, grid, static_cast<cudaStream_t>(d.stream));
+  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+}  // namespace fl
 
 extern "C" {
 
@@ -160,85 +314,12 @@ fl_status fl_sync_status(void* stream) {
 
 fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                       const fl_attn_desc* desc) {
-  if (!desc || !q || !k || !v || !out) return FL_ERR_INVALID_ARG;
-  const fl_attn_desc& d = *desc;
-  if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0) return FL_ERR_INVALID_ARG;
-  if (!(d.d == 32 || d.d == 64 || d.d == 128)) return FL_ERR_UNSUPPORTED;
-  if (d.dv != d.d) return FL_ERR_UNSUPPORTED;
-  if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
-  if (d.mask_kind < FL_MASK_NONE || d.mask_kind > FL_MASK_DOCUMENT) return FL_ERR_INVALID_ARG;
-  if (d.mask_kind != FL_MASK_NONE && d.Lq != d.Lk) return FL_ERR_UNSUPPORTED;
-  if (d.mask_kind == FL_MASK_SLIDING_WINDOW && d.window < 1) return FL_ERR_INVALID_ARG;
-  if (d.mask_kind == FL_MASK_PREFIX_LM && d.prefix_len < 0) return FL_ERR_INVALID_ARG;
-  if (d.mask_kind == FL_MASK_DOCUMENT && (!d.doc_offsets || d.num_docs < 1 || d.num_docs > d.Lq))
-    return FL_ERR_INVALID_ARG;
-  if (d.score_mod < FL_SCORE_NONE || d.score_mod > FL_SCORE_SOFTCAP) return FL_ERR_INVALID_ARG;
-  if (d.score_mod == FL_SCORE_ALIBI && !d.alibi_slopes) return FL_ERR_INVALID_ARG;
-  if (d.score_mod == FL_SCORE_SOFTCAP && !(d.softcap > 0.f && std::isfinite(d.softcap))) return FL_ERR_INVALID_ARG;
-  Strides sq, sk, sv, so;
-  if (!resolve_strides(d.q_strides, d.Hq, d.Lq, d.d, &sq) || !resolve_strides(d.k_strides, d.Hkv, d.Lk, d.d, &sk) ||
-      !resolve_strides(d.v_strides, d.Hkv, d.Lk, d.dv, &sv) || !resolve_strides(d.o_strides, d.Hq, d.Lq, d.dv, &so))
-    return FL_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !strides_aligned(sq) ||
-      !strides_aligned(sk) || !strides_aligned(sv) || !strides_aligned(so))
-    return FL_ERR_ALIGNMENT;
-  if (d.mask_kind == FL_MASK_DOCUMENT && (reinterpret_cast<uintptr_t>(d.doc_offsets) & 3u)) return FL_ERR_ALIGNMENT;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FL_ERR_ALIGNMENT;
-
+  const fl_status chk = fl::attn_fwd_check(q, k, v, out, lse, desc);
+  if (chk != FL_OK) return chk;
   DeviceState* ds = nullptr;
-  fl_status st = device_state(&ds);
+  const fl_status st = device_state(&ds);
   if (st != FL_OK) return st;
-
-  KParams p{};
-  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.Lq = d.Lq; p.Lk = d.Lk;
-  p.group = d.Hq / d.Hkv;
-  p.n_qtiles = (d.Lq + fl::kBlockM - 1) / fl::kBlockM;
-  const float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
-  p.window = d.window; p.prefix = d.prefix_len;
-  p.doc_offsets = d.doc_offsets; p.num_docs = d.num_docs;
-  p.slopes = d.alibi_slopes; p.softcap = d.softcap;
-  p.out = out; p.o_sb = so.b; p.o_sh = so.h; p.o_sl = so.l;
-  p.lse = lse;
-  p.status = ds->status;
-  p.timeout_ns = wait_ns(d.wait_limit_ms);
-  p.dbg_skip_tile = (d.debug_flags & FL_DEBUG_SKIP_KV_LOAD) ? (d.debug_arg < 0 ? 0 : d.debug_arg) : -1;
-#ifdef FL_TRACE
-  if (const char* tp = std::getenv("FLATTN_TRACE_PTR"))
-    p.trace = reinterpret_cast<unsigned long long*>(std::strtoull(tp, nullptr, 0));
-#endif
-  int64_t units;
-  if (p.group == 1) {
-    p.slot_mode = fl::SLOT_ROWS;
-    units = static_cast<int64_t>(d.B) * d.Hq * ((p.n_qtiles + 1) / 2);
-  } else {
-    p.slot_mode = fl::SLOT_HEADS;
-    p.pairs_per_group = (p.group + 1) / 2;
-    units = static_cast<int64_t>(d.B) * d.Hkv * p.pairs_per_group * p.n_qtiles;
-  }
-  if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
-  p.num_units = static_cast<int>(units);
-
-  CUtensorMap maps[6];
-  const int bq = box_width(d.d), bv = box_width(d.dv);
-  if (!encode_bhlc(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sq.l, sq.h, sq.b, bq) ||
-      !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sk.l, sk.h, sk.b, bq) ||
-      !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bv) ||
-      !encode_bhlc(&maps[5], out, d.dv, d.Lq, d.Hq, d.B, so.l, so.h, so.b, bv))
-    return FL_ERR_CUDA;
-  maps[3] = maps[0];
-  maps[4] = maps[1];
-
-  const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
-  cudaStream_t stream = static_cast<cudaStream_t>(d.stream);
-  cudaError_t e;
-  switch (d.d) {
-    case 32: e = fl::launch_attn_d32(d.score_mod, maps, p, grid, stream); break;
-    case 64: e = fl::launch_attn_d64(d.score_mod, maps, p, grid, stream); break;
-    default: e = fl::launch_attn_d128(d.score_mod, maps, p, grid, stream); break;
-  }
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  return fl::attn_fwd_launch(q, k, v, out, lse, desc, ds->status, ds->sm_count);
 }
 
 fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, void* out,
@@ -254,7 +335,7 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
     if (d.q_strides[i] || d.k_strides[i] || d.v_strides[i] || d.o_strides[i]) return FL_ERR_UNSUPPORTED;
   if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
     return FL_ERR_ALIGNMENT;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FL_ERR_ALIGNMENT;
+  if (lse && !aligned4(lse)) return FL_ERR_ALIGNMENT;
 
   DeviceState* ds = nullptr;
   fl_status st = device_state(&ds);
@@ -265,7 +346,8 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
   p.B = d.B; p.Hq = H; p.Hkv = H; p.Lq = L; p.Lk = L; p.group = 1;
   p.n_qtiles = (L + fl::kBlockM - 1) / fl::kBlockM;
   const float scale = d.scale > 0.f ? d.scale : 0.125f;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.scale_log2 = scale * static_cast<float>(kLog2e);
   p.mask_kind = d.mask_kind;
   p.out = out; p.o_sl = 128; p.o_sh = static_cast<int64_t>(L) * 128; p.o_sb = static_cast<int64_t>(H) * L * 128;
   p.lse = lse;
@@ -278,7 +360,7 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
   if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[6];
+  CUtensorMap maps[8];
   const int64_t sl = 64, sh = static_cast<int64_t>(L) * 64, sb = static_cast<int64_t>(H) * L * 64;
   if (!encode_bhlc(&maps[0], q1, 64, L, H, d.B, sl, sh, sb, 64) ||
       !encode_bhlc(&maps[1], k1, 64, L, H, d.B, sl, sh, sb, 64) ||
@@ -289,6 +371,8 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
       !encode_bhlc(&maps[5], out, 128, L, H, d.B, 128, static_cast<int64_t>(L) * 128,
                    static_cast<int64_t>(H) * L * 128, 64))
     return FL_ERR_CUDA;
+  maps[6] = maps[0];
+  maps[7] = maps[0];
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
   cudaError_t e = fl::launch_diff_d64(maps, p, grid, static_cast<cudaStream_t>(d.stream));
   return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
@@ -300,12 +384,11 @@ fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* 
                                       void* stream) {
   if (!q || !k || !v || !gate || !out) return FL_ERR_INVALID_ARG;
   if (B < 1 || N_seq < 1 || N_res < 1 || H < 1 || !std::isfinite(scale)) return FL_ERR_INVALID_ARG;
-  if (d != 32 && d != 64) return FL_ERR_UNSUPPORTED;
+  if (d != 32) return FL_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gate) || !aligned16(out)) return FL_ERR_ALIGNMENT;
-  if ((pair_bias && (reinterpret_cast<uintptr_t>(pair_bias) & 15u)) ||
-      (mask_bias && (reinterpret_cast<uintptr_t>(mask_bias) & 15u)) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+  if ((pair_bias && !aligned16(pair_bias)) || (mask_bias && !aligned16(mask_bias)) || (lse && !aligned4(lse)))
     return FL_ERR_ALIGNMENT;
-  if ((pair_bias || mask_bias) && (N_res % 4) != 0) return FL_ERR_UNSUPPORTED;  // float4 bias rows
+  if ((pair_bias || mask_bias) && (N_res % 4) != 0) return FL_ERR_UNSUPPORTED;  // 16-byte bias rows
 
   DeviceState* ds = nullptr;
   fl_status st = device_state(&ds);
@@ -316,20 +399,25 @@ fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* 
   p.B = static_cast<int>(Bf); p.Hq = H; p.Hkv = H; p.Lq = N_res; p.Lk = N_res; p.group = 1;
   p.n_qtiles = (N_res + fl::kBlockM - 1) / fl::kBlockM;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
-  p.scale_log2 = sc * 1.4426950408889634f;
+  p.scale = sc;
+  p.scale_log2 = sc * static_cast<float>(kLog2e);
   p.mask_kind = fl::MASK_NONE;
   p.out = out; p.o_sl = d; p.o_sh = static_cast<int64_t>(N_res) * d; p.o_sb = static_cast<int64_t>(H) * N_res * d;
   p.lse = lse;
-  p.pair_bias = pair_bias; p.mask_bias = mask_bias; p.gate = gate; p.n_seq = N_seq;
+  p.gate = gate;
+  p.evo_b = B; p.evo_h = H; p.evo_n = N_seq;
+  p.has_pb = pair_bias != nullptr;
+  p.has_mb = mask_bias != nullptr;
   p.status = ds->status;
   p.timeout_ns = kDefaultWaitNs;
   p.dbg_skip_tile = -1;
-  p.slot_mode = fl::SLOT_ROWS;
-  const int64_t units = Bf * H * ((p.n_qtiles + 1) / 2);
+  p.slot_mode = fl::SLOT_PAIR;
+  p.chunked = 1;
+  const int64_t units = static_cast<int64_t>(B) * H * p.n_qtiles * ((N_seq + 1) / 2);
   if (units > 0x7fffffff || Bf > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
 
-  CUtensorMap maps[6];
+  CUtensorMap maps[8];
   const int bw = box_width(d);
   const int64_t sl = d, sh = static_cast<int64_t>(N_res) * d, sb = static_cast<int64_t>(H) * N_res * d;
   if (!encode_bhlc(&maps[0], q, d, N_res, H, Bf, sl, sh, sb, bw) ||
@@ -339,8 +427,69 @@ fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* 
     return FL_ERR_CUDA;
   maps[3] = maps[0];
   maps[4] = maps[1];
+  maps[6] = maps[0];
+  maps[7] = maps[0];
+  if (pair_bias && !encode_pair_bias(&maps[6], pair_bias, B, H, N_res)) return FL_ERR_CUDA;
+  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, Bf, N_res)) return FL_ERR_CUDA;
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
-  cudaError_t e = fl::launch_evo(d, maps, p, grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e = fl::launch_evo_row(maps, p, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+fl_status fl_evoformer_col_gated_attn_fwd(const void* q, const void* k, const void* v, const float* mask_bias,
+                                          const void* gate, void* out, float* lse, int32_t B, int32_t N_seq,
+                                          int32_t N_res, int32_t H, int32_t d, float scale, void* stream) {
+  if (!q || !k || !v || !gate || !out) return FL_ERR_INVALID_ARG;
+  if (B < 1 || N_seq < 1 || N_res < 1 || H < 1 || !std::isfinite(scale)) return FL_ERR_INVALID_ARG;
+  if (d != 32 && d != 64) return FL_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gate) || !aligned16(out)) return FL_ERR_ALIGNMENT;
+  if ((mask_bias && !aligned16(mask_bias)) || (lse && !aligned4(lse))) return FL_ERR_ALIGNMENT;
+  if (mask_bias && (N_seq % 4) != 0) return FL_ERR_UNSUPPORTED;  // 16-byte bias rows
+
+  DeviceState* ds = nullptr;
+  fl_status st = device_state(&ds);
+  if (st != FL_OK) return st;
+
+  // heads of the kernel: (h, r) with stride d; rows: MSA rows s with stride H * N_res * d
+  const int64_t HR = static_cast<int64_t>(H) * N_res;
+  if (HR > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  KParams p{};
+  p.B = B; p.Hq = static_cast<int>(HR); p.Hkv = p.Hq; p.Lq = N_seq; p.Lk = N_seq; p.group = 1;
+  p.n_qtiles = (N_seq + fl::kBlockM - 1) / fl::kBlockM;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  p.scale = sc;
+  p.scale_log2 = sc * static_cast<float>(kLog2e);
+  p.mask_kind = fl::MASK_NONE;
+  const int64_t sl = HR * d, sh = d, sb = static_cast<int64_t>(N_seq) * HR * d;
+  p.out = out; p.o_sl = sl; p.o_sh = sh; p.o_sb = sb;
+  p.lse = lse;
+  p.gate = gate;
+  p.evo_b = B; p.evo_h = H; p.evo_n = N_res;
+  p.has_pb = 0;
+  p.has_mb = mask_bias != nullptr;
+  p.status = ds->status;
+  p.timeout_ns = kDefaultWaitNs;
+  p.dbg_skip_tile = -1;
+  p.slot_mode = fl::SLOT_PAIR;
+  p.chunked = 1;
+  const int64_t units = static_cast<int64_t>(B) * H * ((N_res + 1) / 2) * p.n_qtiles;
+  if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+
+  CUtensorMap maps[8];
+  const int bw = box_width(d);
+  if (!encode_bhlc(&maps[0], q, d, N_seq, HR, B, sl, sh, sb, bw) ||
+      !encode_bhlc(&maps[1], k, d, N_seq, HR, B, sl, sh, sb, bw) ||
+      !encode_bhlc(&maps[2], v, d, N_seq, HR, B, sl, sh, sb, bw) ||
+      !encode_bhlc(&maps[5], out, d, N_seq, HR, B, sl, sh, sb, bw))
+    return FL_ERR_CUDA;
+  maps[3] = maps[0];
+  maps[4] = maps[1];
+  maps[6] = maps[0];
+  maps[7] = maps[0];
+  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, static_cast<int64_t>(B) * N_res, N_seq)) return FL_ERR_CUDA;
+  const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
+  cudaError_t e = fl::launch_evo_col(d, maps, p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 

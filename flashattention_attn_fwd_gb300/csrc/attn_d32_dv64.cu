@@ -1,0 +1,8 @@
+// Fused attention forward, head dim 32, value head dim 64 (vanilla / ALiBi / softcap score, any mask).
+#include "launch.cuh"
+
+namespace fl {
+cudaError_t launch_attn_d32_dv64(int score_mod, const CUtensorMap* maps, const KParams& p, int grid, cudaStream_t s) {
+  return launch_attn_by_score<32, 64>(score_mod, maps, p, grid, s);
+}
+}  // namespace fl

@@ -6,31 +6,58 @@
 
 namespace fl {
 
-enum Kind : int { KIND_ATTN = 0, KIND_DIFF = 1, KIND_EVO = 2 };
+// KIND_ATTN    : softmax(score_mod(scale QK^T) + mask) V, MHA / GQA
+// KIND_DIFF    : differential attention (two Q/K branches, one V)
+// KIND_EVO     : Evoformer MSA row-wise gated attention (pair bias shared by
+//                the MSA rows, residue mask bias, sigmoid gate)
+// KIND_EVO_COL : Evoformer MSA column-wise gated attention (attention over
+//                the MSA rows of each residue column, mask bias, gate)
+enum Kind : int { KIND_ATTN = 0, KIND_DIFF = 1, KIND_EVO = 2, KIND_EVO_COL = 3 };
 enum ScoreMod : int { SCORE_NONE = 0, SCORE_ALIBI = 1, SCORE_SOFTCAP = 2 };
 enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_WINDOW = 2, MASK_PREFIX = 3, MASK_DOC = 4 };
 
 // How the two query tiles ("slots") of one work unit are chosen.
-//   SLOT_ROWS   : query row tiles 2t and 2t+1 of one head (MHA, Evoformer)
+//   SLOT_ROWS   : query row tiles 2t and 2t+1 of one head (MHA)
 //   SLOT_HEADS  : the same row tile of two query heads of one GQA group
 //   SLOT_BRANCH : the same rows of the two branches of differential attention
-enum SlotMode : int { SLOT_ROWS = 0, SLOT_HEADS = 1, SLOT_BRANCH = 2 };
+//   SLOT_PAIR   : the same rows of two independent problems with their own
+//                 K/V (Evoformer: two MSA rows, or two residue columns)
+enum SlotMode : int { SLOT_ROWS = 0, SLOT_HEADS = 1, SLOT_BRANCH = 2, SLOT_PAIR = 3 };
 
 constexpr int kBlockM = 128;  // query rows per slot (one TMEM lane per row)
 constexpr int kBlockN = 128;  // keys per key/value tile
-// warp 0: TMA; warps 1 and 10: MMA issue for slot 0 / slot 1; warps 2-9:
-// softmax (4 warps per slot)
-constexpr int kThreads = 352;
+// Softmax threads per query row (1: each thread holds a whole 128-score row;
+// 2: two threads per row, each with half of it, exchanging their maxima).
+#ifndef FL_ROW_SPLIT
+#define FL_ROW_SPLIT 1
+#endif
+constexpr int kRowSplit = FL_ROW_SPLIT;
+static_assert(kRowSplit == 1 || kRowSplit == 2, "threads per row");
+constexpr int kHalfCols = kBlockN / kRowSplit;  // scores of one row held by one softmax thread
+// Warpgroup 0 = warp 0 TMA, warps 1 / 2 MMA issue, warp 3 idle; then the
+// softmax warpgroups of slot 0 and of slot 1 (4 * kRowSplit warps each).
+constexpr int kSoftmaxWarps = 8 * kRowSplit;
+constexpr int kThreads = 128 + 32 * kSoftmaxWarps;
+// Registers per thread: at launch (65536 / kThreads rounded down to a
+// multiple of 8), then after setmaxnreg for the control warpgroup and the
+// softmax warpgroups; their total stays within the launch's.
+constexpr int kLaunchRegs = kRowSplit == 1 ? 168 : 96;
+constexpr int kCtlRegs = kRowSplit == 1 ? 56 : 32;
+constexpr int kSoftmaxRegs = kRowSplit == 1 ? 224 : 112;
+static_assert(128 * kCtlRegs + 32 * kSoftmaxWarps * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 
 struct KParams {
-  // problem (for the Evoformer, B is B * N_seq and Hq == Hkv == H)
+  // problem (Evoformer row-wise: B is B * N_seq, Hq == Hkv == H;
+  // column-wise: Hq == Hkv == H * N_res, rows are MSA rows)
   int B, Hq, Hkv, Lq, Lk;
   int group;            // Hq / Hkv
   int n_qtiles;         // ceil(Lq / 128)
   int slot_mode;
   int pairs_per_group;  // SLOT_HEADS: ceil(group / 2)
   int num_units;
+  int chunked;          // 1: each CTA takes a contiguous range of units
   float scale_log2;     // scale * log2(e)
+  float scale;          // scale (natural units; Evoformer)
 
   // mask
   int mask_kind, doc_causal, window, prefix;
@@ -40,6 +67,10 @@ struct KParams {
   // score mod
   const float* slopes;  // ALiBi slopes, natural units
   float softcap;
+  // softcap on the FMA pipe: x = s * (q0 + q1 s^2 + q2 s^4 + q3 s^6) (log2
+  // units) while |s| <= sc_smax
+  float sc_q[4];
+  float sc_smax;
 
   // outputs; out strides in elements for (b, h, l), channel stride 1
   void* out;
@@ -50,16 +81,17 @@ struct KParams {
   float lambda;
 
   // Evoformer
-  const float* pair_bias;   // [Bb, H, Nr, Nr]
-  const float* mask_bias;   // [Bb * N_seq, Nr]
-  const void* gate;         // same layout as out
-  int n_seq;
+  int evo_b;            // batch of the Evoformer call
+  int evo_h;            // heads H
+  int evo_n;            // the paired axis: N_seq (row-wise) or N_res (column-wise)
+  int has_pb, has_mb;
+  const void* gate;     // same layout as out
 
   // control
-  uint32_t* status;         // device status word (bit 0: timeout), [1]: where
+  uint32_t* status;     // device status word (bit 0: timeout), [1]: where
   uint64_t timeout_ns;
-  int dbg_skip_tile;        // < 0: off
-  // Phase timestamps of block 0 (builds with -DFL_TRACE only): [role 4][tile 64][event 8]
+  int dbg_skip_tile;    // < 0: off
+  // Phase timestamps of block 0 (builds with -DFL_TRACE only): [role 6][tile 64][event 8]
   unsigned long long* trace;
 };
 

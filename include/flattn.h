@@ -114,9 +114,10 @@ FL_API void fl_attn_desc_init(fl_attn_desc* desc);
 /*
  * Fused attention forward, variants V1-V8: vanilla MHA, GQA, ALiBi, tanh
  * softcap, causal, sliding window, prefix-LM, document mask (score_mod and
- * mask compose).  Supported: d in {32, 64, 128}, dv == d, Hq % Hkv == 0,
- * any Lq, Lk >= 1 (ragged tails are masked inside the kernel).  Fully masked
- * key tiles are skipped from the descriptor alone (no block mask is built).
+ * mask compose).  Supported: d and dv each in {32, 64, 128} (dv may differ
+ * from d), Hq % Hkv == 0, any Lq, Lk >= 1 (ragged tails are masked inside
+ * the kernel).  Fully masked key tiles are skipped from the descriptor alone
+ * (no block mask is built).
  */
 FL_API fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                       const fl_attn_desc* desc);
@@ -136,20 +137,42 @@ FL_API fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2,
 
 /*
  * AlphaFold Evoformer MSA row-wise gated self-attention (the Flashlight wiki
- * summary, 设计取舍, notes its extra broadcast bias dimension):
+ * summary, 设计取舍, notes its extra broadcast bias dimension; technical
+ * summary, Results, names the row-wise form):
  *   t[i,j] = scale q_i.k_j + pair_bias[b,h,i,j] + mask_bias[b,s,j]
  *   out    = sigmoid(gate) * softmax_j(t) V
- * q, k, v, gate, out : bf16 [B, N_seq, H, N_res, d] contiguous, d in {32, 64}
+ * q, k, v, gate, out : bf16 [B, N_seq, H, N_res, d] contiguous, d = 32
+ *                      (AlphaFold's per-head width)
  * pair_bias          : fp32 [B, H, N_res, N_res] (shared by all N_seq rows), or NULL
  * mask_bias          : fp32 [B, N_seq, N_res] (e.g. 0 / -1e9), or NULL
  * lse                : fp32 [B, N_seq, H, N_res], or NULL
- * scale <= 0 selects 1/sqrt(d).
+ * With a bias, N_res must be a multiple of 4 (16-byte bias rows), else
+ * FL_ERR_UNSUPPORTED.  scale <= 0 selects 1/sqrt(d).
  */
 FL_API fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* v,
                                       const float* pair_bias, const float* mask_bias,
                                       const void* gate, void* out, float* lse, int32_t B,
                                       int32_t N_seq, int32_t N_res, int32_t H, int32_t d,
                                       float scale, void* stream);
+
+/*
+ * AlphaFold Evoformer MSA column-wise gated self-attention (the Flashlight
+ * technical summary, Results, names the column-wise form beside the
+ * row-wise one): for every residue column r, attention over the MSA rows,
+ *   t[s,s'] = scale q[b,s,h,r].k[b,s',h,r] + mask_bias[b,r,s']
+ *   out[b,s,h,r] = sigmoid(gate[b,s,h,r]) * sum_s' softmax_s'(t[s,.]) v[b,s',h,r]
+ * q, k, v, gate, out : bf16 [B, N_seq, H, N_res, d] contiguous (the same
+ *                      layout as the row-wise call), d in {32, 64}
+ * mask_bias          : fp32 [B, N_res, N_seq] (the MSA mask of each residue
+ *                      column as an additive 0 / -1e9 bias), or NULL; N_seq
+ *                      must then be a multiple of 4
+ * lse                : fp32 [B, H, N_res, N_seq], or NULL
+ * No pair bias enters the column-wise form.  scale <= 0 selects 1/sqrt(d).
+ */
+FL_API fl_status fl_evoformer_col_gated_attn_fwd(const void* q, const void* k, const void* v,
+                                          const float* mask_bias, const void* gate, void* out,
+                                          float* lse, int32_t B, int32_t N_seq, int32_t N_res,
+                                          int32_t H, int32_t d, float scale, void* stream);
 
 /*
  * Allocation-free variant of fl_attn_fwd (no counterpart in the paper; it is

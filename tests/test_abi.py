@@ -66,7 +66,8 @@ def _attn(L, desc, q=P, k=P, v=P, o=P, lse=0):
     (dict(Hq=3, Hkv=2), _lib.FL_ERR_INVALID_ARG),
     (dict(Lq=0), _lib.FL_ERR_INVALID_ARG),
     (dict(d=96, dv=96), _lib.FL_ERR_UNSUPPORTED),
-    (dict(dv=32), _lib.FL_ERR_UNSUPPORTED),
+    (dict(dv=96), _lib.FL_ERR_UNSUPPORTED),
+    (dict(dv=256), _lib.FL_ERR_UNSUPPORTED),
     (dict(mask_kind=9), _lib.FL_ERR_INVALID_ARG),
     (dict(mask_kind=1, Lk=64), _lib.FL_ERR_UNSUPPORTED),
     (dict(mask_kind=2, window=0), _lib.FL_ERR_INVALID_ARG),
@@ -120,6 +121,18 @@ def test_evoformer_rejects(L):
     assert f(P, P, P, P + 4, P, P, P, 0, 1, 4, 256, 8, 32, s, None) == _lib.FL_ERR_ALIGNMENT
     assert f(P, P, P, P, P, P, P, 0, 1, 4, 250, 8, 32, s, None) == _lib.FL_ERR_UNSUPPORTED
     assert f(P, P, P, P, P, P, P, 0, 1, 4, 256, 8, 32, ctypes.c_float(float("inf")), None) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, P, P, 0, 1, 4, 256, 8, 64, s, None) == _lib.FL_ERR_UNSUPPORTED  # row-wise: d = 32
+
+
+def test_evoformer_col_rejects(L):
+    f = L.fl_evoformer_col_gated_attn_fwd
+    s = ctypes.c_float(0.0)
+    assert f(P, P, P, P, 0, P, 0, 1, 128, 256, 8, 32, s, None) == _lib.FL_ERR_INVALID_ARG  # no gate
+    assert f(P, P, P, P, P, P, 0, 1, 128, 256, 8, 48, s, None) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, 0, 1, 0, 256, 8, 32, s, None) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P, P + 4, P, P, 0, 1, 128, 256, 8, 32, s, None) == _lib.FL_ERR_ALIGNMENT
+    assert f(P, P, P, P, P, P, 0, 1, 126, 256, 8, 32, s, None) == _lib.FL_ERR_UNSUPPORTED  # N_seq % 4 with a mask
+    assert f(P, P, P, P, P, P, P + 2, 1, 128, 256, 8, 32, s, None) == _lib.FL_ERR_ALIGNMENT
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import oracle
-from flashattention_attn_fwd_gb300 import (FlattnError, attn_fwd, diffattn_fwd, evoformer_gated_attn_fwd,
-                                           synth, sync_status)
+from flashattention_attn_fwd_gb300 import (FlattnError, attn_fwd, diffattn_fwd, evoformer_col_gated_attn_fwd,
+                                           evoformer_gated_attn_fwd, synth, sync_status)
 from flashattention_attn_fwd_gb300._lib import FL_DEBUG_SKIP_KV_LOAD, FL_ERR_TIMEOUT
 
 pytestmark = pytest.mark.gpu
@@ -57,8 +57,8 @@ def _oracle_kw(kw, offs=None, slopes=None):
     return o
 
 
-def run_attn(B, Hq, Hkv, L, d, seed=0, n_docs=None, **kw):
-    q, k, v = synth.attn_inputs(B, Hq, Hkv, L, d, seed=seed)
+def run_attn(B, Hq, Hkv, L, d, seed=0, n_docs=None, dv=None, **kw):
+    q, k, v = synth.attn_inputs(B, Hq, Hkv, L, d, dv=dv, seed=seed)
     offs = synth.doc_offsets(B, L, n_docs, seed=seed) if n_docs else None
     slopes = synth.alibi_slopes(Hq) if kw.get("score_mod") == "alibi" else None
     gkw = dict(kw)
@@ -123,6 +123,55 @@ def test_attn_small_elementwise(case):
     check(out, ro, lse, rl)
 
 
+DV_CASES = [
+    # (B, Hq, Hkv, L, d, dv, kwargs): value head dim different from the query/key one
+    (1, 2, 2, 300, 64, 128, dict(mask="causal")),
+    (2, 8, 2, 300, 64, 128, dict(mask="causal")),
+    (1, 2, 2, 300, 64, 128, dict(score_mod="alibi")),
+    (1, 2, 2, 200, 32, 64, dict(mask="causal")),
+    (1, 4, 2, 200, 32, 128, dict()),
+    (1, 2, 2, 200, 128, 64, dict(mask="window", window=70)),
+    (1, 2, 2, 300, 64, 32, dict(score_mod="softcap", softcap=5.0)),
+    (1, 2, 2, 260, 128, 32, dict(mask="prefix_lm", prefix=50)),
+]
+
+
+@pytest.mark.parametrize("case", DV_CASES, ids=lambda c: f"B{c[0]}H{c[1]}x{c[2]}L{c[3]}d{c[4]}dv{c[5]}-" +
+                         "-".join(f"{k}{v}" for k, v in c[6].items()))
+def test_attn_value_head_dim_differs(case):
+    B, Hq, Hkv, L, d, dv, kw = case
+    (q, k, v, offs, slopes), out, lse = run_attn(B, Hq, Hkv, L, d, seed=L + dv, dv=dv, **kw)
+    assert out.shape == (B, Hq, L, dv)
+    ro, rl = oracle.attention(q, k, v, **_oracle_kw(kw, offs, slopes))
+    check(out, ro, lse, rl)
+
+
+MULTI_UNIT = [
+    # more work units than SMs, so each CTA runs several units back to back
+    (2, 16, 16, 1280, 128, dict(mask="causal")),
+    (2, 16, 16, 1280, 128, dict()),
+    (2, 16, 16, 1280, 32, dict(mask="causal")),
+    (2, 16, 16, 1280, 32, dict(score_mod="alibi")),
+    (2, 16, 16, 1280, 64, dict(mask="window", window=200)),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_UNIT, ids=lambda c: f"B{c[0]}H{c[1]}L{c[3]}d{c[4]}-" +
+                         "-".join(f"{k}{v}" for k, v in c[5].items()))
+def test_attn_many_units_per_cta_sampled_rows(case):
+    B, Hq, Hkv, L, d, kw = case
+    (q, k, v, offs, slopes), out, lse = run_attn(B, Hq, Hkv, L, d, seed=7 + d, **kw)
+    rng = np.random.default_rng(d)
+    rows = [(int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(L))) for _ in range(48)]
+    rows += [(0, 0, 0), (B - 1, Hq - 1, L - 1), (1, 3, 127), (1, 5, 128), (0, 9, 1151), (1, 15, 1152)]
+    ro, rl = oracle.attention_rows(q, k, v, rows, **_oracle_kw(kw, offs, slopes))
+    oc, lc = out.float().cpu(), lse.cpu()
+    g = np.stack([oc[b, h, i].numpy() for b, h, i in rows]).astype(np.float64)
+    gl = np.array([lc[b, h, i].item() for b, h, i in rows])
+    assert np.abs(g - ro).max() <= ATOL and np.linalg.norm(g - ro) / np.linalg.norm(ro) <= RTOL
+    assert np.abs(gl - rl).max() <= LSE_ATOL
+
+
 def test_causal_row0_is_v0_bit_exact():
     (q, k, v, _, _), out, _ = run_attn(2, 4, 4, 300, 64, seed=5, mask="causal")
     assert torch.equal(out[:, :, 0].cpu(), v[:, :, 0])
@@ -174,8 +223,9 @@ def test_diffattn_small(B, H, L, causal, lam):
 
 # ----------------------------------------------------------------- Evoformer
 @pytest.mark.parametrize("B,Ns,Nr,H,d,use_pb,use_mb", [(1, 3, 256, 2, 32, True, True), (2, 2, 100, 3, 32, True, True),
-                                                         (1, 2, 300, 2, 32, False, True), (1, 2, 64, 2, 64, True, False),
-                                                         (1, 4, 256, 8, 32, True, True)])
+                                                         (1, 2, 300, 2, 32, False, True), (1, 2, 64, 2, 32, True, False),
+                                                         (1, 4, 256, 8, 32, True, True), (1, 5, 20, 1, 32, False, False),
+                                                         (2, 7, 388, 3, 32, True, True)])
 def test_evoformer_small(B, Ns, Nr, H, d, use_pb, use_mb):
     q, k, v, pb, mb, g = synth.evo_inputs(B, Ns, Nr, H, d=d, seed=Nr + d)
     out, lse = evoformer_gated_attn_fwd(*_gpu(q, k, v), pb.to(DEV) if use_pb else None,
@@ -183,6 +233,18 @@ def test_evoformer_small(B, Ns, Nr, H, d, use_pb, use_mb):
     sync_status()
     ro, rl = oracle.evoformer_gated_attention(q, k, v, pb if use_pb else np.zeros((B, H, Nr, Nr)),
                                               mb if use_mb else np.zeros((B, Ns, Nr)), g)
+    check(out, ro, lse, rl)
+
+
+@pytest.mark.parametrize("B,Ns,Nr,H,d,use_mb", [(1, 16, 8, 2, 32, True), (1, 128, 12, 3, 32, True),
+                                                 (2, 20, 7, 2, 32, True), (1, 200, 6, 2, 32, True),
+                                                 (1, 64, 5, 2, 64, True), (1, 33, 4, 2, 32, False),
+                                                 (1, 132, 9, 2, 64, False)])
+def test_evoformer_col_small(B, Ns, Nr, H, d, use_mb):
+    q, k, v, mb, g = synth.evo_col_inputs(B, Ns, Nr, H, d=d, seed=Ns + Nr + d)
+    out, lse = evoformer_col_gated_attn_fwd(*_gpu(q, k, v), mb.to(DEV) if use_mb else None, g.to(DEV))
+    sync_status()
+    ro, rl = oracle.evoformer_col_gated_attention(q, k, v, mb if use_mb else np.zeros((B, Nr, Ns)), g)
     check(out, ro, lse, rl)
 
 
