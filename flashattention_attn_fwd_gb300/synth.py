@@ -22,6 +22,7 @@ __all__ = [
     "diff_inputs",
     "evo_inputs",
     "evo_col_inputs",
+    "decode_inputs",
 ]
 
 
@@ -131,3 +132,18 @@ def evo_col_inputs(B: int, N_seq: int, N_res: int, H: int, d: int = 32, seed: in
     mask_bias = torch.where(keep, torch.zeros((), dtype=torch.float32),
                             torch.full((), mask_value, dtype=torch.float32))
     return q, k, v, mask_bias, gate
+
+
+def decode_inputs(B: int, Hq: int, Hkv: int, Lq: int, Lmax: int, d: int, seed: int = 0,
+                  min_len: int | None = None):
+    """Decode-phase inputs: q [B,Hq,Lq,d], a key/value cache k, v
+    [B,Hkv,Lmax,d] (bf16 N(0,1)) and int32 kv_len [B], the valid cache length
+    of each sequence, uniform in [min_len, Lmax] (a mixed-length serving
+    batch; default min_len = Lmax // 4, never below Lq)."""
+    g = generator(seed)
+    q = randn_bf16((B, Hq, Lq, d), g)
+    k = randn_bf16((B, Hkv, Lmax, d), g)
+    v = randn_bf16((B, Hkv, Lmax, d), g)
+    lo = max(Lq, Lmax // 4 if min_len is None else min_len)
+    kv_len = torch.randint(lo, Lmax + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return q, k, v, kv_len

@@ -44,6 +44,12 @@ readings taken here are:
                rows s with t = s + mask_bias[r, s'] and no pair bias;
                out = sigmoid(gate) * (P V) (technical summary, Results, names
                the row- and column-wise gated forms).
+* Decode      Lq new query rows against a cache of kv_len[b] keys (the rows
+               are the last Lq positions of that sequence): keys j < kv_len[b]
+               are visible, and with the causal mask only j <= kv_len[b]-Lq+i
+               (technical summary, Methodology, and the wiki summary's
+               批判性分析 note on the serving path's decode phase; the pages
+               evaluate no decode workload, so this is the plain reading).
 * A row with no visible key gives O = 0 and LSE = -inf.
 
 All arithmetic is float64 NumPy; a matmul and ``exp``/``log``/``tanh`` are
@@ -68,6 +74,7 @@ __all__ = [
     "evoformer_rows",
     "evoformer_col_gated_attention",
     "evoformer_col_rows",
+    "decode_attention",
 ]
 
 MASKS = ("none", "causal", "window", "prefix_lm", "document")
@@ -342,3 +349,43 @@ def evoformer_col_rows(q, k, v, mask_bias, gate, rows, *, scale=None):
         outs.append(_sigmoid(gate[b, s, h, r]) * (P @ v[b, :, h, r])[0])
         lses.append(l[0])
     return np.array(outs), np.array(lses)
+
+
+def decode_attention(q, k, v, kv_len=None, *, causal: bool = False, scale: float | None = None,
+                     score_mod: str = "none", slopes=None, softcap: float | None = None):
+    """Decode-phase attention over a key/value cache.
+
+    q [B,Hq,Lq,d]; k [B,Hkv,Lmax,d]; v [B,Hkv,Lmax,dv]; kv_len [B] valid
+    cache lengths (None: Lmax for every sequence).  Query row i of sequence
+    b sits at position p_i = kv_len[b] - Lq + i; key j is visible when
+    j < kv_len[b] and, with ``causal``, j <= p_i.  ALiBi adds m_h (j - p_i).
+    Returns (out [B,Hq,Lq,dv], lse [B,Hq,Lq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lmax = k.shape[1], k.shape[2]
+    dv = v.shape[-1]
+    grp = Hq // Hkv
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    lens = np.full(B, Lmax, dtype=np.int64) if kv_len is None else np.asarray(_f64(kv_len), dtype=np.int64)
+    slopes = None if slopes is None else _f64(slopes)
+    out = np.zeros((B, Hq, Lq, dv))
+    lse = np.zeros((B, Hq, Lq))
+    for b in range(B):
+        n = int(lens[b])
+        pos = n - Lq + np.arange(Lq)[:, None]
+        j = np.arange(Lmax)[None, :]
+        vis = j < n
+        if causal:
+            vis = vis & (j <= pos)
+        for h in range(Hq):
+            g = h // grp
+            s = scale * (q[b, h] @ k[b, g].T)
+            if score_mod == "alibi":
+                s = s + slopes[h] * (j - pos)
+            elif score_mod == "softcap":
+                s = float(softcap) * np.tanh(s / float(softcap))
+            t = np.where(vis, s, -np.inf)
+            P, l = softmax_rows(t)
+            out[b, h] = P @ v[b, g]
+            lse[b, h] = l
+    return out, lse

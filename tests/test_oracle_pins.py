@@ -372,6 +372,77 @@ def test_brute_force_evoformer():
                 assert lse[0, s, h, i] == pytest.approx(l, abs=1e-12)
 
 
+def test_decode_reduces_to_prefix_attention():
+    """One new row with the whole cache visible is vanilla attention over
+    the first kv_len keys; Lq rows with the causal mask and kv_len == Lq is
+    causal self-attention; ALiBi is measured from the row's own position."""
+    B, Hq, Hkv, Lq, Lmax, d = 3, 4, 2, 1, 20, 8
+    q, k, v = _rand(B, Hq, Lq, d), _rand(B, Hkv, Lmax, d), _rand(B, Hkv, Lmax, d)
+    lens = np.array([20, 7, 1])
+    out, lse = oracle.decode_attention(q, k, v, lens)
+    for b in range(B):
+        n = lens[b]
+        ro, rl = oracle.attention(q[b:b + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n])
+        np.testing.assert_allclose(out[b:b + 1], ro, atol=1e-13)
+        np.testing.assert_allclose(lse[b:b + 1], rl, atol=1e-13)
+    Lq = 5
+    q2 = _rand(B, Hq, Lq, d)
+    out, lse = oracle.decode_attention(q2, k[:, :, :Lq], v[:, :, :Lq], np.full(B, Lq), causal=True)
+    ro, rl = oracle.attention(q2, k[:, :, :Lq], v[:, :, :Lq], mask="causal")
+    np.testing.assert_allclose(out, ro, atol=1e-13)
+    np.testing.assert_allclose(lse, rl, atol=1e-13)
+
+
+def test_decode_causal_offset_and_sdpa_crosscheck():
+    """Bottom-right causal alignment against torch SDPA (float64) with an
+    explicit boolean mask, plus the q = 0 closed form: the last row sees
+    kv_len keys, row i sees kv_len - Lq + i + 1."""
+    B, Hq, Hkv, Lq, Lmax, d = 2, 4, 2, 3, 16, 8
+    q, k, v = _rand(B, Hq, Lq, d), _rand(B, Hkv, Lmax, d), _rand(B, Hkv, Lmax, d)
+    lens = np.array([16, 9])
+    out, lse = oracle.decode_attention(q, k, v, lens, causal=True)
+    for b in range(B):
+        n = lens[b]
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lmax)[None, :]
+        m = (j < n) & (j <= n - Lq + i)
+        ref = _sdpa(q[b:b + 1], np.repeat(k[b:b + 1], 2, axis=1), np.repeat(v[b:b + 1], 2, axis=1), attn_mask=m)
+        np.testing.assert_allclose(out[b:b + 1], ref, atol=1e-12)
+    out0, lse0 = oracle.decode_attention(np.zeros_like(q), k, v, lens, causal=True)
+    for b in range(B):
+        for i in range(Lq):
+            cnt = lens[b] - Lq + i + 1
+            np.testing.assert_allclose(lse0[b, :, i], math.log(cnt), atol=1e-12)
+            np.testing.assert_allclose(out0[b, 0, i], v[b, 0, :cnt].mean(0), atol=1e-12)
+
+
+def test_brute_force_decode():
+    B, Hq, Hkv, Lq, Lmax, d = 2, 2, 1, 2, 9, 4
+    q, k, v = _rand(B, Hq, Lq, d), _rand(B, Hkv, Lmax, d), _rand(B, Hkv, Lmax, d)
+    lens = np.array([9, 4])
+    slopes = np.array([0.5, 0.125])
+    for kw in (dict(), dict(causal=True), dict(score_mod="alibi", slopes=slopes, causal=True),
+               dict(score_mod="softcap", softcap=1.5)):
+        out, lse = oracle.decode_attention(q, k, v, lens, scale=0.4, **kw)
+        for b in range(B):
+            n = int(lens[b])
+            for h in range(Hq):
+                for i in range(Lq):
+                    p = n - Lq + i
+                    K = k[b, 0, :n].tolist()
+                    V = v[b, 0, :n].tolist()
+                    # brute_row's causal is j <= row index: pass the position
+                    mk = dict(mask="causal") if kw.get("causal") else {}
+                    sm = {}
+                    if kw.get("score_mod") == "alibi":
+                        sm = dict(score_mod="alibi", slope=float(slopes[h]))
+                    elif kw.get("score_mod") == "softcap":
+                        sm = dict(score_mod="softcap", cap=1.5)
+                    o, l = brute_row(q[b, h, i].tolist(), K, V, p, 0.4, **mk, **sm)
+                    np.testing.assert_allclose(out[b, h, i], o, atol=1e-12)
+                    assert lse[b, h, i] == pytest.approx(l, abs=1e-12)
+
+
 def test_evoformer_col_is_row_form_on_transposed_msa():
     """Column-wise attention over MSA rows = the (separately pinned) row-wise
     form on the MSA with its two axes swapped, with zero pair bias and the
