@@ -161,6 +161,8 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flashattention_attn_fwd_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -224,6 +226,41 @@ def variant_configs():
             return call, tf, ef, by, "1 input set (271 MB > L2)"
         return "4 diffattn B4 H16 L4096 causal lambda0.8", build
 
+    def evo_col():
+        def build():
+            sets = []
+            for s_ in range(2):
+                e = [x.to(dev) for x in synth.evo_col_inputs(1, 128, 256, 8, d=32, seed=70 + s_)]
+                sets.append((e, torch.empty_like(e[0]), torch.empty(1, 8, 256, 128, device=dev)))
+            tf, ef, by = F.evo_col_counts(1, 128, 256, 8)
+            it = [0]
+
+            def call():
+                e, o, lse = sets[it[0] % 2]
+                it[0] += 1
+                api.evoformer_col_gated_attn_fwd(*e, out=o, lse=lse)
+            return call, tf, ef, by, "2 rotating input sets (170 MB > L2)"
+        return "5col evoformer-column Ns128 Nr256 H8 d32", build
+
+    def decode():
+        def build():
+            q, k, v, kv_len = synth.decode_inputs(16, 32, 8, 1, 8192, 64, seed=61)
+            q, k, v, kv_len = q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev)
+            o = torch.empty_like(q)
+            lse = torch.empty(16, 32, 1, device=dev)
+            tf, ef, by = F.decode_counts(16, 32, 8, 1, 64, kv_len.cpu().numpy())
+            from flashattention_attn_fwd_gb300 import _lib
+            import ctypes
+            desc = _lib.new_desc()
+            desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = 16, 32, 8, 1, 8192, 64, 64
+            need = int(_lib.lib().fl_attn_decode_workspace_size(ctypes.byref(desc)))
+            ws = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+
+            def call():
+                api.attn_decode_fwd(q, k, v, kv_len, out=o, lse=lse, workspace=ws)
+            return call, tf, ef, by, "1 input set (269 MB cache > L2)"
+        return "6 decode B16 Hq32 Hkv8 Lq1 cache8192 d64 mixed-lengths", build
+
     def evo():
         def build():
             sets = []
@@ -249,6 +286,8 @@ def variant_configs():
         attn("3b gqa32/8 prefix1024 B2 L8192 d64", 2, 32, 8, 8192, 64, 2, 13, mask="prefix_lm", prefix=1024),
         diff(),
         evo(),
+        evo_col(),
+        decode(),
     ]
 
 
@@ -305,6 +344,27 @@ def _oracle_head(args):
         okw["slopes"] = synth.alibi_slopes(H)[h:h + 1]
     oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], **okw)
     return 1
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def git_sha():
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "--short=12", "HEAD"], capture_output=True, text=True,
+                           timeout=5)
+        return r.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        return None
 
 
 def oracle_sample(n_heads: int, seed: int = 0):
@@ -378,8 +438,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"score_mod MHA fwd B={B} H={H} L={L} d={D}: ALiBi, softcap 30, "
                                "causal window 256", "sample_per_step": f"{n_heads} heads x 3 variants"},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": workers, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                         "workers": workers, "cpu_model": cpu_model(), "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -528,8 +588,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, wall, workers, desc = oracle_sample(n_heads=8)
-        cpu = {"value": round(v, 6), "unit": UNIT, "cores": workers, "kind": "oracle", "sample": desc,
-               "wall_s": round(wall, 2)}
+        cpu = {"value": round(v, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "workers": workers,
+               "cpu_model": cpu_model(), "kind": "oracle", "sample": desc, "wall_s": round(wall, 2)}
 
     if rank == 0:
         line = {
@@ -548,6 +608,7 @@ def main():
             "gpu_launches": K * len(HEADLINE),
             "clocks": clocks,
             "variants": variants,
+            "git_sha": git_sha(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

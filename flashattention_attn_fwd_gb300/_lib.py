@@ -36,6 +36,8 @@ EXPORTS = (
     "fl_abi_version",
     "fl_attn_desc_size",
     "fl_attn_fwd_noalloc",
+    "fl_attn_decode_fwd",
+    "fl_attn_decode_workspace_size",
 )
 
 
@@ -89,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.fl_evoformer_gated_attn_fwd.restype = i32
         L.fl_evoformer_col_gated_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
         L.fl_evoformer_col_gated_attn_fwd.restype = i32
+        L.fl_attn_decode_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(AttnDesc)]
+        L.fl_attn_decode_fwd.restype = i32
+        L.fl_attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
+        L.fl_attn_decode_workspace_size.restype = ctypes.c_size_t
         L.fl_sync_status.argtypes = [vp]
         L.fl_sync_status.restype = i32
         L.fl_status_string.argtypes = [i32]

@@ -185,6 +185,51 @@ def evoformer_col_gated_attn_fwd(q, k, v, mask_bias, gate, *, scale: float | Non
     return out, lse
 
 
+def attn_decode_fwd(q, k_cache, v_cache, kv_len=None, *, causal: bool = False, score_mod: str = "none",
+                    alibi_slopes=None, softcap: float | None = None, scale: float | None = None,
+                    out=None, lse=None, return_lse: bool = True, workspace=None, stream=None):
+    """fl_attn_decode_fwd: q [B,Hq,Lq,d], k_cache/v_cache [B,Hkv,Lk,d] bf16
+    contiguous, kv_len int32 [B] (or None).  The key-split workspace is
+    allocated with torch when not given.  Returns (out [B,Hq,Lq,d] bf16,
+    lse [B,Hq,Lq] fp32 or None)."""
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Hq, Lq, d = q.shape
+    _, Hkv, Lk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 4)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Lq), device=q.device, dtype=torch.float32)
+    if kv_len is not None:
+        _need(kv_len, "kv_len", 1, torch.int32)
+    desc = _lib.new_desc()
+    desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = B, Hq, Hkv, Lq, Lk, d, v_cache.shape[-1]
+    desc.scale = 0.0 if scale is None else float(scale)
+    desc.mask_kind = MASKS["causal" if causal else "none"]
+    if score_mod not in SCORE_MODS:
+        raise ValueError(f"unknown score_mod {score_mod!r}")
+    desc.score_mod = SCORE_MODS[score_mod]
+    desc.softcap = 0.0 if softcap is None else float(softcap)
+    if alibi_slopes is not None:
+        _need(alibi_slopes, "alibi_slopes", 1, torch.float32)
+        desc.alibi_slopes = alibi_slopes.data_ptr()
+    desc.stream = _stream_ptr(stream)
+    need = int(_lib.lib().fl_attn_decode_workspace_size(ctypes.byref(desc)))
+    if need and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_ptr = 0 if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.lib().fl_attn_decode_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                       0 if lse is None else lse.data_ptr(),
+                                       0 if kv_len is None else kv_len.data_ptr(),
+                                       ws_ptr, ctypes.c_size_t(ws_bytes), ctypes.byref(desc))
+    _lib.check(st, "fl_attn_decode_fwd")
+    return out, lse
+
+
 def sync_status(stream=None) -> int:
     """fl_sync_status: synchronise the stream and return (and clear) the
     device status word; raises FlattnError if a kernel reported a failure."""

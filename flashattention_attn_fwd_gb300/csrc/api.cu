@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "decode.h"
 #include "flattn.h"
 #include "host.h"
 #include "kernels.h"
@@ -320,6 +321,81 @@ fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   const fl_status st = device_state(&ds);
   if (st != FL_OK) return st;
   return fl::attn_fwd_launch(q, k, v, out, lse, desc, ds->status, ds->sm_count);
+}
+
+namespace {
+
+fl_status decode_check(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* kv_len,
+                       const fl_attn_desc* desc) {
+  if (!desc || !q || !k || !v || !out) return FL_ERR_INVALID_ARG;
+  const fl_attn_desc& d = *desc;
+  if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0 || d.Lq > d.Lk)
+    return FL_ERR_INVALID_ARG;
+  if (d.d != d.dv || (d.d != 64 && d.d != 128)) return FL_ERR_UNSUPPORTED;
+  if ((d.Hq / d.Hkv) * d.Lq > fl::kDecodeMaxRows) return FL_ERR_UNSUPPORTED;
+  if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind != FL_MASK_NONE && d.mask_kind != FL_MASK_CAUSAL) return FL_ERR_UNSUPPORTED;
+  if (d.score_mod < FL_SCORE_NONE || d.score_mod > FL_SCORE_SOFTCAP) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_ALIBI && !d.alibi_slopes) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_SOFTCAP && !(d.softcap > 0.f && std::isfinite(d.softcap))) return FL_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (d.q_strides[i] || d.k_strides[i] || d.v_strides[i] || d.o_strides[i]) return FL_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FL_ERR_ALIGNMENT;
+  if ((lse && !aligned4(lse)) || (kv_len && !aligned4(kv_len))) return FL_ERR_ALIGNMENT;
+  return FL_OK;
+}
+
+size_t decode_workspace(const fl_attn_desc& d, int sm_count, int* n_split, int* chunk) {
+  fl::decode_split(d.B, d.Hkv, d.Lk, sm_count, n_split, chunk);
+  if (*n_split <= 1) return 0;
+  const size_t rows = static_cast<size_t>(d.B) * d.Hq * d.Lq;
+  return static_cast<size_t>(*n_split) * rows * (static_cast<size_t>(d.d) + 1) * sizeof(float);
+}
+
+}  // namespace
+
+size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc) {
+  if (!desc || desc->B < 1 || desc->Hkv < 1 || desc->Lk < 1) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != FL_OK) return 0;
+  int ns = 1, chunk = 0;
+  return decode_workspace(*desc, ds->sm_count, &ns, &chunk);
+}
+
+fl_status fl_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                             const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                             const fl_attn_desc* desc) {
+  const fl_status chk = decode_check(q, k_cache, v_cache, out, lse, kv_len, desc);
+  if (chk != FL_OK) return chk;
+  const fl_attn_desc& d = *desc;
+  DeviceState* ds = nullptr;
+  const fl_status st = device_state(&ds);
+  if (st != FL_OK) return st;
+  fl::DecodeParams p{};
+  const size_t need = decode_workspace(d, ds->sm_count, &p.n_split, &p.chunk);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return FL_ERR_INVALID_ARG;
+  if (need > 0 && !aligned16(workspace)) return FL_ERR_ALIGNMENT;
+  p.q = q; p.out = out; p.lse = lse; p.kv_len = kv_len; p.slopes = d.alibi_slopes;
+  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.Lq = d.Lq; p.Lmax = d.Lk;
+  p.rows = static_cast<int64_t>(d.B) * d.Hq * d.Lq;
+  if (need > 0) {
+    p.opart = static_cast<float*>(workspace);
+    p.lpart = p.opart + static_cast<int64_t>(p.n_split) * p.rows * d.d;
+  }
+  p.scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
+  p.softcap = d.softcap;
+  p.score_mod = d.score_mod;
+  p.causal = d.mask_kind == FL_MASK_CAUSAL;
+  p.status = ds->status;
+  p.timeout_ns = wait_ns(d.wait_limit_ms);
+  if (static_cast<int64_t>(d.B) * d.Hkv * p.n_split > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  CUtensorMap maps[2];
+  const int64_t sl = d.d, sh = static_cast<int64_t>(d.Lk) * d.d, sb = static_cast<int64_t>(d.Hkv) * d.Lk * d.d;
+  if (!encode_bhlc(&maps[0], k_cache, d.d, d.Lk, d.Hkv, d.B, sl, sh, sb, 64) ||
+      !encode_bhlc(&maps[1], v_cache, d.d, d.Lk, d.Hkv, d.B, sl, sh, sb, 64))
+    return FL_ERR_CUDA;
+  const cudaError_t e = fl::launch_decode(d.d, maps, p, static_cast<cudaStream_t>(d.stream));
+  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
 fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, void* out,

@@ -97,6 +97,35 @@ def evo_counts(B, N_seq, N_res, H, d=32, with_pair_bias=True, with_mask=True):
     return tile_flops, exact_flops, bytes_
 
 
+def evo_col_counts(B, N_seq, N_res, H, d=32, with_mask=True):
+    """Column-wise Evoformer: attention over the N_seq MSA rows of each of the
+    B * H * N_res residue columns; no pair bias."""
+    lo, hi = row_intervals("none", N_seq)
+    tiles, pairs = visible_tiles(lo, hi, N_seq), visible_pairs(lo, hi)
+    per_pair = 4 * d
+    n = B * H * N_res
+    tile_flops = n * tiles * TILE * TILE * per_pair
+    exact_flops = n * pairs * per_pair
+    bytes_ = 2 * 5 * n * N_seq * d + 4 * n * N_seq
+    if with_mask:
+        bytes_ += 4 * B * N_res * N_seq
+    return tile_flops, exact_flops, bytes_
+
+
+def decode_counts(B, Hq, Hkv, Lq, d, kv_len, causal=False):
+    """Decode over a key/value cache: the FLOPs of the visible (row, key)
+    pairs (no tile rounding: the kernel has no 128-row tiles) and the bytes
+    of q, the valid part of the K/V cache, out and lse."""
+    lens = np.asarray(kv_len, dtype=np.int64)
+    if causal:
+        pairs = int(sum(sum(n - Lq + i + 1 for i in range(Lq)) for n in lens))
+    else:
+        pairs = int(lens.sum()) * Lq
+    flops = pairs * Hq * 4 * d
+    bytes_ = 2 * (2 * B * Hq * Lq * d + 2 * int(lens.sum()) * Hkv * d) + 4 * B * Hq * Lq
+    return flops, flops, bytes_
+
+
 def roofline_time(flops: float, bytes_: float, tflops_peak: float, hbm_gbs: float):
     """(seconds, bound) of the slower of tensor-peak and HBM-peak time."""
     t_tensor = flops / (tflops_peak * 1e12)

@@ -34,6 +34,7 @@
 #ifndef FLATTN_H_
 #define FLATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -173,6 +174,35 @@ FL_API fl_status fl_evoformer_col_gated_attn_fwd(const void* q, const void* k, c
                                           const float* mask_bias, const void* gate, void* out,
                                           float* lse, int32_t B, int32_t N_seq, int32_t N_res,
                                           int32_t H, int32_t d, float scale, void* stream);
+
+/*
+ * Decode-phase attention over a key/value cache (the Flashlight wiki
+ * summary's critical analysis, 批判性分析, names the serving path's decode
+ * phase; the technical summary's online softmax is applied per key split):
+ * Lq new query rows per sequence against the first kv_len[b] cached keys.
+ * Query row i of sequence b sits at position p = kv_len[b] - Lq + i; key j
+ * is visible when j < kv_len[b] and, with mask_kind CAUSAL, j <= p.  ALiBi
+ * adds alibi_slopes[h] * (j - p); softcap as in fl_attn_fwd.
+ *   q, out            : bf16 [B, Hq, Lq, d] contiguous
+ *   k_cache, v_cache  : bf16 [B, Hkv, Lk, d] contiguous (desc->Lk = cache capacity)
+ *   lse               : fp32 [B, Hq, Lq] or NULL
+ *   kv_len            : device int32 [B] (values clamped to [0, Lk]), or NULL for Lk
+ *   workspace         : caller-owned device buffer of at least
+ *                       fl_attn_decode_workspace_size(desc) bytes (16-byte
+ *                       aligned; may be NULL when that size is 0)
+ * desc: d == dv in {64, 128}; (Hq / Hkv) * Lq <= 64; Lq <= Lk; mask NONE or
+ * CAUSAL; strides zero.  The key axis is split over CTAs so that the grid
+ * covers the GPU; each split's normalised partial output and log-sum-exp go
+ * to the workspace and a second kernel merges them.  Rows that see no key
+ * get out = 0 and lse = -inf.
+ */
+FL_API fl_status fl_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* out,
+                                    float* lse, const int32_t* kv_len, void* workspace,
+                                    size_t workspace_bytes, const fl_attn_desc* desc);
+
+/* Workspace bytes fl_attn_decode_fwd needs for `desc` on the current device
+   (0 when the key axis is not split, or on an invalid descriptor). */
+FL_API size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc);
 
 /*
  * Allocation-free variant of fl_attn_fwd (no counterpart in the paper; it is

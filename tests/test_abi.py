@@ -135,6 +135,39 @@ def test_evoformer_col_rejects(L):
     assert f(P, P, P, P, P, P, P + 2, 1, 128, 256, 8, 32, s, None) == _lib.FL_ERR_ALIGNMENT
 
 
+def test_decode_rejects(L):
+    f = L.fl_attn_decode_fwd
+    def dd(**kw):
+        base = dict(B=2, Hq=8, Hkv=2, Lq=1, Lk=4096, d=64, dv=64)
+        base.update(kw)
+        return _desc(**base)
+    z = ctypes.c_size_t(0)
+    assert f(P, P, P, P, 0, 0, 0, z, None) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, 0, P, P, 0, 0, 0, z, ctypes.byref(dd())) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(d=32, dv=32))) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(dv=128))) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(Hq=64, Hkv=1, Lq=2))) == _lib.FL_ERR_UNSUPPORTED  # 128 rows
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(mask_kind=2, window=8))) == _lib.FL_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(Lq=8, Lk=4))) == _lib.FL_ERR_INVALID_ARG
+    assert f(P, P, P + 8, P, 0, 0, 0, z, ctypes.byref(dd())) == _lib.FL_ERR_ALIGNMENT
+    assert f(P, P, P, P, 0, P + 2, 0, z, ctypes.byref(dd())) == _lib.FL_ERR_ALIGNMENT
+    assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(score_mod=1))) == _lib.FL_ERR_INVALID_ARG
+
+
+def test_decode_split_arithmetic():
+    """Host split rule (mirrors csrc/decode.h): enough CTAs for twice the
+    SMs, every split a whole number of 128-key tiles, no empty split."""
+    def split(B, Hkv, Lmax, sms):
+        tiles = (Lmax + 127) // 128
+        ns = max(1, min(tiles, -(-2 * sms // (B * Hkv))))
+        per = -(-tiles // ns)
+        return -(-tiles // per), per * 128
+    for B, Hkv, Lmax in ((16, 8, 8192), (1, 1, 100), (2, 8, 65536), (64, 8, 1024)):
+        ns, chunk = split(B, Hkv, Lmax, 152)
+        assert chunk % 128 == 0 and (ns - 1) * chunk < Lmax <= ns * chunk
+    assert split(1, 1, 100, 152) == (1, 128)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_cuda_error(L):
     assert _attn(L, _desc()) == _lib.FL_ERR_CUDA
