@@ -261,6 +261,20 @@ def variant_configs():
             return call, tf, ef, by, "1 input set (269 MB cache > L2)"
         return "6 decode B16 Hq32 Hkv8 Lq1 cache8192 d64 mixed-lengths", build
 
+    def bwd(name, Bb, Hh, Ll, d, seed, **kw):
+        def build():
+            q, k, v = (t.to(dev) for t in synth.attn_inputs(Bb, Hh, Hh, Ll, d, seed=seed))
+            dout = synth.randn_bf16((Bb, Hh, Ll, d), synth.generator(seed + 1)).to(dev)
+            out, lse = api.attn_fwd(q, k, v, **kw)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(Bb * Hh * Ll * (d + 2) * 4, device=dev, dtype=torch.uint8)
+            tf, ef, by = F.bwd_counts(Bb, Hh, Hh, Ll, d, **kw)
+
+            def call():
+                api.attn_bwd(q, k, v, out, dout, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            return call, tf, ef, by, "1 input set (100 MB of inputs and outputs; dq accumulator 67 MB)"
+        return name, build
+
     def evo():
         def build():
             sets = []
@@ -288,6 +302,7 @@ def variant_configs():
         evo(),
         evo_col(),
         decode(),
+        bwd("7 backward B4 H16 L2048 d64 causal", 4, 16, 2048, 64, 90, mask="causal"),
     ]
 
 

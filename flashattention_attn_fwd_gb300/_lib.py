@@ -38,6 +38,9 @@ EXPORTS = (
     "fl_attn_fwd_noalloc",
     "fl_attn_decode_fwd",
     "fl_attn_decode_workspace_size",
+    "fl_attn_bwd",
+    "fl_attn_bwd_workspace_size",
+    "fl_last_error_detail",
 )
 
 
@@ -63,7 +66,10 @@ class AttnDesc(ctypes.Structure):
 class FlattnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        detail = ""
+        if status == FL_ERR_CUDA:
+            detail = lib().fl_last_error_detail().decode()
+        super().__init__(f"{what}: {status_string(status)} (status {status})" + (f" [{detail}]" if detail else ""))
 
 
 _lib = None
@@ -95,8 +101,14 @@ def lib() -> ctypes.CDLL:
         L.fl_attn_decode_fwd.restype = i32
         L.fl_attn_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
         L.fl_attn_decode_workspace_size.restype = ctypes.c_size_t
+        L.fl_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(AttnDesc)]
+        L.fl_attn_bwd.restype = i32
+        L.fl_attn_bwd_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
+        L.fl_attn_bwd_workspace_size.restype = ctypes.c_size_t
         L.fl_sync_status.argtypes = [vp]
         L.fl_sync_status.restype = i32
+        L.fl_last_error_detail.argtypes = []
+        L.fl_last_error_detail.restype = ctypes.c_char_p
         L.fl_status_string.argtypes = [i32]
         L.fl_status_string.restype = ctypes.c_char_p
         L.fl_abi_version.argtypes = []

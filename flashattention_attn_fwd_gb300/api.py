@@ -37,6 +37,33 @@ def _strides4(t: torch.Tensor):
     return (ctypes.c_int64 * 4)(*[int(x) for x in s])
 
 
+def _variant_desc(B, Hq, Hkv, Lq, Lk, d, dv, *, mask="none", window=None, prefix=None, doc_offsets=None,
+                  doc_causal=False, score_mod="none", alibi_slopes=None, softcap=None, scale=None):
+    desc = _lib.new_desc()
+    desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = B, Hq, Hkv, Lq, Lk, d, dv
+    desc.scale = 0.0 if scale is None else float(scale)
+    if mask not in MASKS:
+        raise ValueError(f"unknown mask {mask!r}")
+    desc.mask_kind = MASKS[mask]
+    desc.doc_causal = 1 if doc_causal else 0
+    desc.window = 0 if window is None else int(window)
+    desc.prefix_len = 0 if prefix is None else int(prefix)
+    if score_mod not in SCORE_MODS:
+        raise ValueError(f"unknown score_mod {score_mod!r}")
+    desc.score_mod = SCORE_MODS[score_mod]
+    desc.softcap = 0.0 if softcap is None else float(softcap)
+    if alibi_slopes is not None:
+        _need(alibi_slopes, "alibi_slopes", 1, torch.float32)
+        desc.alibi_slopes = alibi_slopes.data_ptr()
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", 2, torch.int32)
+        if not doc_offsets.is_contiguous():
+            raise ValueError("doc_offsets must be contiguous")
+        desc.doc_offsets = doc_offsets.data_ptr()
+        desc.num_docs = doc_offsets.shape[1] - 1
+    return desc
+
+
 def attn_fwd(q, k, v, *, mask: str = "none", window: int | None = None, prefix: int | None = None,
              doc_offsets: torch.Tensor | None = None, doc_causal: bool = False,
              score_mod: str = "none", alibi_slopes: torch.Tensor | None = None,
@@ -62,28 +89,9 @@ def attn_fwd(q, k, v, *, mask: str = "none", window: int | None = None, prefix: 
         _need(lse, "lse", 3, torch.float32)
         if not lse.is_contiguous():
             raise ValueError("lse must be contiguous")
-    desc = _lib.new_desc()
-    desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = B, Hq, Hkv, Lq, Lk, d, dv
-    desc.scale = 0.0 if scale is None else float(scale)
-    if mask not in MASKS:
-        raise ValueError(f"unknown mask {mask!r}")
-    desc.mask_kind = MASKS[mask]
-    desc.doc_causal = 1 if doc_causal else 0
-    desc.window = 0 if window is None else int(window)
-    desc.prefix_len = 0 if prefix is None else int(prefix)
-    if score_mod not in SCORE_MODS:
-        raise ValueError(f"unknown score_mod {score_mod!r}")
-    desc.score_mod = SCORE_MODS[score_mod]
-    desc.softcap = 0.0 if softcap is None else float(softcap)
-    if alibi_slopes is not None:
-        _need(alibi_slopes, "alibi_slopes", 1, torch.float32)
-        desc.alibi_slopes = alibi_slopes.data_ptr()
-    if doc_offsets is not None:
-        _need(doc_offsets, "doc_offsets", 2, torch.int32)
-        if not doc_offsets.is_contiguous():
-            raise ValueError("doc_offsets must be contiguous")
-        desc.doc_offsets = doc_offsets.data_ptr()
-        desc.num_docs = doc_offsets.shape[1] - 1
+    desc = _variant_desc(B, Hq, Hkv, Lq, Lk, d, dv, mask=mask, window=window, prefix=prefix,
+                         doc_offsets=doc_offsets, doc_causal=doc_causal, score_mod=score_mod,
+                         alibi_slopes=alibi_slopes, softcap=softcap, scale=scale)
     desc.q_strides, desc.k_strides = _strides4(q), _strides4(k)
     desc.v_strides, desc.o_strides = _strides4(v), _strides4(out)
     desc.stream = _stream_ptr(stream)
@@ -228,6 +236,57 @@ def attn_decode_fwd(q, k_cache, v_cache, kv_len=None, *, causal: bool = False, s
                                        ws_ptr, ctypes.c_size_t(ws_bytes), ctypes.byref(desc))
     _lib.check(st, "fl_attn_decode_fwd")
     return out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, *, mask: str = "none", window: int | None = None,
+             prefix: int | None = None, doc_offsets: torch.Tensor | None = None, doc_causal: bool = False,
+             score_mod: str = "none", alibi_slopes: torch.Tensor | None = None, softcap: float | None = None,
+             scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """fl_attn_bwd: gradients (dq, dk, dv) of attn_fwd given its out, lse and
+    dout; contiguous bf16 tensors, the forward's variant arguments."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _need(t, name, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _need(lse, "lse", 3, torch.float32)
+    B, Hq, Lq, d = q.shape
+    _, Hkv, Lk, _ = k.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    desc = _variant_desc(B, Hq, Hkv, Lq, Lk, d, v.shape[-1], mask=mask, window=window, prefix=prefix,
+                         doc_offsets=doc_offsets, doc_causal=doc_causal, score_mod=score_mod,
+                         alibi_slopes=alibi_slopes, softcap=softcap, scale=scale)
+    desc.stream = _stream_ptr(stream)
+    need = int(_lib.lib().fl_attn_bwd_workspace_size(ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    st = _lib.lib().fl_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                                ctypes.c_size_t(workspace.numel() * workspace.element_size()), ctypes.byref(desc))
+    _lib.check(st, "fl_attn_bwd")
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, kw):
+        out, lse = attn_fwd(q, k, v, **kw)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.kw = kw
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, out, dout.contiguous(), lse, **ctx.kw)
+        return dq, dk, dv, None
+
+
+def attention(q, k, v, **kw):
+    """Differentiable fused attention: attn_fwd in the forward, attn_bwd in
+    the backward (the variant keyword arguments of attn_fwd)."""
+    return _Attention.apply(q, k, v, kw)
 
 
 def sync_status(stream=None) -> int:

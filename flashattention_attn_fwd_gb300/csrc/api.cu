@@ -5,9 +5,11 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
+#include "bwd.h"
 #include "decode.h"
 #include "flattn.h"
 #include "host.h"
@@ -46,6 +48,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Detail of the last FL_ERR_CUDA on this thread (fl_last_error_detail).
+thread_local char g_detail[192] = "";
+
+fl_status cuda_fail(const char* where, cudaError_t e) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s", where, e == cudaSuccess ? "failed" : cudaGetErrorString(e));
+  return FL_ERR_CUDA;
+}
+
+fl_status launched(const char* where, cudaError_t e) {
+  return e == cudaSuccess ? FL_OK : cuda_fail(where, e);
+}
+
 struct DeviceState {
   int sm_count = 0;
   uint32_t* status = nullptr;  // [0]: error bits, [1]: where the wait gave up
@@ -56,18 +70,26 @@ DeviceState g_dev[kMaxDevices];
 
 fl_status device_state(DeviceState** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FL_ERR_CUDA;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail("cudaGetDevice", ge);
+  // make the device's primary context current on this thread (a thread that
+  // has made no runtime call yet, e.g. an autograd worker, has none, and the
+  // tensor-map encoder is a driver call)
+  const cudaError_t sd = cudaSetDevice(dev);
+  if (sd != cudaSuccess) return cuda_fail("cudaSetDevice", sd);
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& d = g_dev[dev];
   if (d.status == nullptr) {
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-      return FL_ERR_CUDA;
+    const cudaError_t ae = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (ae != cudaSuccess || sms <= 0) return cuda_fail("cudaDeviceGetAttribute", ae);
     uint32_t* st = nullptr;
-    if (cudaMalloc(&st, 4 * sizeof(uint32_t)) != cudaSuccess) return FL_ERR_CUDA;
-    if (cudaMemset(st, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
+    const cudaError_t me = cudaMalloc(&st, 4 * sizeof(uint32_t));
+    if (me != cudaSuccess) return cuda_fail("cudaMalloc (status word)", me);
+    const cudaError_t se = cudaMemset(st, 0, 4 * sizeof(uint32_t));
+    if (se != cudaSuccess) {
       cudaFree(st);
-      return FL_ERR_CUDA;
+      return cuda_fail("cudaMemset (status word)", se);
     }
     d.sm_count = sms;
     d.status = st;
@@ -259,16 +281,15 @@ fl_status attn_fwd_launch(const void* q, const void* k, const void* v, void* out
       !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sk.l, sk.h, sk.b, bq) ||
       !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, sv.l, sv.h, sv.b, bv) ||
       !encode_bhlc(&maps[5], out, d.dv, d.Lq, d.Hq, d.B, so.l, so.h, so.b, bv))
-    return FL_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
   maps[3] = maps[0];
   maps[4] = maps[1];
   maps[6] = maps[0];
   maps[7] = maps[0];
 
   const int grid = static_cast<int>(units < sm_count ? units : sm_count);
-  const cudaError_t e =
-      launch_attn(d.d, d.dv, d.score_mod, maps, p, grid, static_cast<cudaStream_t>(d.stream));
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  return launched("attention kernel launch",
+                  launch_attn(d.d, d.dv, d.score_mod, maps, p, grid, static_cast<cudaStream_t>(d.stream)));
 }
 
 }  // namespace fl
@@ -299,17 +320,22 @@ const char* fl_status_string(fl_status s) {
 
 int32_t fl_abi_version(void) { return FL_ABI_VERSION; }
 
+const char* fl_last_error_detail(void) { return g_detail; }
+
 int32_t fl_attn_desc_size(void) { return static_cast<int32_t>(sizeof(fl_attn_desc)); }
 
 fl_status fl_sync_status(void* stream) {
   DeviceState* ds = nullptr;
   fl_status st = device_state(&ds);
   if (st != FL_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FL_ERR_CUDA;
+  const cudaError_t se = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (se != cudaSuccess) return cuda_fail("cudaStreamSynchronize", se);
   uint32_t h[2] = {0u, 0u};
-  if (cudaMemcpy(h, ds->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FL_ERR_CUDA;
+  const cudaError_t ce = cudaMemcpy(h, ds->status, sizeof(h), cudaMemcpyDeviceToHost);
+  if (ce != cudaSuccess) return cuda_fail("cudaMemcpy (status word)", ce);
   if (h[0] == 0u) return FL_OK;
-  if (cudaMemset(ds->status, 0, 2 * sizeof(uint32_t)) != cudaSuccess) return FL_ERR_CUDA;
+  const cudaError_t me = cudaMemset(ds->status, 0, 2 * sizeof(uint32_t));
+  if (me != cudaSuccess) return cuda_fail("cudaMemset (status word)", me);
   return (h[0] & 1u) ? FL_ERR_TIMEOUT : FL_ERR_DEVICE_BOUNDS;
 }
 
@@ -354,6 +380,75 @@ size_t decode_workspace(const fl_attn_desc& d, int sm_count, int* n_split, int* 
 
 }  // namespace
 
+size_t fl_attn_bwd_workspace_size(const fl_attn_desc* desc) {
+  if (!desc || desc->B < 1 || desc->Hq < 1 || desc->Lq < 1 || desc->d < 1) return 0;
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Hq * desc->Lq;
+  return rows * (static_cast<size_t>(desc->d) + 2) * sizeof(float);
+}
+
+fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      const fl_attn_desc* desc) {
+  if (!desc || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FL_ERR_INVALID_ARG;
+  const fl_attn_desc& d = *desc;
+  if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0) return FL_ERR_INVALID_ARG;
+  if (d.d != d.dv || (d.d != 32 && d.d != 64)) return FL_ERR_UNSUPPORTED;
+  if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind < FL_MASK_NONE || d.mask_kind > FL_MASK_DOCUMENT) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind != FL_MASK_NONE && d.Lq != d.Lk) return FL_ERR_UNSUPPORTED;
+  if (d.mask_kind == FL_MASK_SLIDING_WINDOW && d.window < 1) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind == FL_MASK_PREFIX_LM && d.prefix_len < 0) return FL_ERR_INVALID_ARG;
+  if (d.mask_kind == FL_MASK_DOCUMENT && (!d.doc_offsets || d.num_docs < 1 || d.num_docs > d.Lq))
+    return FL_ERR_INVALID_ARG;
+  if (d.score_mod < FL_SCORE_NONE || d.score_mod > FL_SCORE_SOFTCAP) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_ALIBI && !d.alibi_slopes) return FL_ERR_INVALID_ARG;
+  if (d.score_mod == FL_SCORE_SOFTCAP && !(d.softcap > 0.f && std::isfinite(d.softcap))) return FL_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (d.q_strides[i] || d.k_strides[i] || d.v_strides[i] || d.o_strides[i]) return FL_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, out, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FL_ERR_ALIGNMENT;
+  if (!aligned4(lse) || (d.mask_kind == FL_MASK_DOCUMENT && !aligned4(d.doc_offsets))) return FL_ERR_ALIGNMENT;
+  if (d.Lq % 4 != 0) return FL_ERR_UNSUPPORTED;  // 16-byte rows of the per-query vectors (TMA)
+  const size_t need = fl_attn_bwd_workspace_size(desc);
+  if (!workspace || workspace_bytes < need) return FL_ERR_INVALID_ARG;
+
+  DeviceState* ds = nullptr;
+  const fl_status st = device_state(&ds);
+  if (st != FL_OK) return st;
+  fl::BwdParams p{};
+  p.out = out; p.dout = dout; p.lse = lse; p.dq = dq; p.dk = dk; p.dv = dv;
+  p.rows = static_cast<int64_t>(d.B) * d.Hq * d.Lq;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.dvec = p.dq_acc + p.rows * d.d;
+  p.l2 = p.dvec + p.rows;
+  p.slopes = d.alibi_slopes; p.doc_offsets = d.doc_offsets;
+  p.status = ds->status;
+  p.timeout_ns = wait_ns(d.wait_limit_ms);
+  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.Lq = d.Lq; p.Lk = d.Lk;
+  p.n_ktiles = (d.Lk + 127) / 128;
+  p.scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
+  p.softcap = d.softcap;
+  p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
+  p.window = d.window; p.prefix = d.prefix_len; p.num_docs = d.num_docs;
+  if (static_cast<int64_t>(d.B) * d.Hkv * p.n_ktiles > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  CUtensorMap maps[6];
+  const int bw = box_width(d.d);
+  const int64_t sl = d.d;
+  if (!encode_bhlc(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sl, static_cast<int64_t>(d.Lq) * d.d,
+                   static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
+      !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sl, static_cast<int64_t>(d.Lk) * d.d,
+                   static_cast<int64_t>(d.Hkv) * d.Lk * d.d, bw) ||
+      !encode_bhlc(&maps[2], v, d.d, d.Lk, d.Hkv, d.B, sl, static_cast<int64_t>(d.Lk) * d.d,
+                   static_cast<int64_t>(d.Hkv) * d.Lk * d.d, bw) ||
+      !encode_bhlc(&maps[3], dout, d.d, d.Lq, d.Hq, d.B, sl, static_cast<int64_t>(d.Lq) * d.d,
+                   static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
+      !encode_rows_f32(&maps[4], p.l2, static_cast<int64_t>(d.B) * d.Hq, d.Lq) ||
+      !encode_rows_f32(&maps[5], p.dvec, static_cast<int64_t>(d.B) * d.Hq, d.Lq))
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
+  return launched("backward kernel launch", fl::launch_bwd(d.d, d.score_mod, maps, p, static_cast<cudaStream_t>(d.stream)));
+}
+
 size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc) {
   if (!desc || desc->B < 1 || desc->Hkv < 1 || desc->Lk < 1) return 0;
   DeviceState* ds = nullptr;
@@ -393,9 +488,8 @@ fl_status fl_attn_decode_fwd(const void* q, const void* k_cache, const void* v_c
   const int64_t sl = d.d, sh = static_cast<int64_t>(d.Lk) * d.d, sb = static_cast<int64_t>(d.Hkv) * d.Lk * d.d;
   if (!encode_bhlc(&maps[0], k_cache, d.d, d.Lk, d.Hkv, d.B, sl, sh, sb, 64) ||
       !encode_bhlc(&maps[1], v_cache, d.d, d.Lk, d.Hkv, d.B, sl, sh, sb, 64))
-    return FL_ERR_CUDA;
-  const cudaError_t e = fl::launch_decode(d.d, maps, p, static_cast<cudaStream_t>(d.stream));
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
+  return launched("decode kernel launch", fl::launch_decode(d.d, maps, p, static_cast<cudaStream_t>(d.stream)));
 }
 
 fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, void* out,
@@ -446,12 +540,11 @@ fl_status fl_diffattn_fwd(const void* q1, const void* k1, const void* q2, const 
       !encode_bhlc(&maps[4], k2, 64, L, H, d.B, sl, sh, sb, 64) ||
       !encode_bhlc(&maps[5], out, 128, L, H, d.B, 128, static_cast<int64_t>(L) * 128,
                    static_cast<int64_t>(H) * L * 128, 64))
-    return FL_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
   maps[6] = maps[0];
   maps[7] = maps[0];
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
-  cudaError_t e = fl::launch_diff_d64(maps, p, grid, static_cast<cudaStream_t>(d.stream));
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  return launched("differential attention launch", fl::launch_diff_d64(maps, p, grid, static_cast<cudaStream_t>(d.stream)));
 }
 
 fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* v, const float* pair_bias,
@@ -500,16 +593,17 @@ fl_status fl_evoformer_gated_attn_fwd(const void* q, const void* k, const void* 
       !encode_bhlc(&maps[1], k, d, N_res, H, Bf, sl, sh, sb, bw) ||
       !encode_bhlc(&maps[2], v, d, N_res, H, Bf, sl, sh, sb, bw) ||
       !encode_bhlc(&maps[5], out, d, N_res, H, Bf, sl, sh, sb, bw))
-    return FL_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
   maps[3] = maps[0];
   maps[4] = maps[1];
   maps[6] = maps[0];
   maps[7] = maps[0];
-  if (pair_bias && !encode_pair_bias(&maps[6], pair_bias, B, H, N_res)) return FL_ERR_CUDA;
-  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, Bf, N_res)) return FL_ERR_CUDA;
+  if (pair_bias && !encode_pair_bias(&maps[6], pair_bias, B, H, N_res))
+    return cuda_fail("cuTensorMapEncodeTiled (pair bias)", cudaSuccess);
+  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, Bf, N_res))
+    return cuda_fail("cuTensorMapEncodeTiled (mask bias)", cudaSuccess);
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
-  cudaError_t e = fl::launch_evo_row(maps, p, grid, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  return launched("Evoformer kernel launch", fl::launch_evo_row(maps, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
 fl_status fl_evoformer_col_gated_attn_fwd(const void* q, const void* k, const void* v, const float* mask_bias,
@@ -558,15 +652,15 @@ fl_status fl_evoformer_col_gated_attn_fwd(const void* q, const void* k, const vo
       !encode_bhlc(&maps[1], k, d, N_seq, HR, B, sl, sh, sb, bw) ||
       !encode_bhlc(&maps[2], v, d, N_seq, HR, B, sl, sh, sb, bw) ||
       !encode_bhlc(&maps[5], out, d, N_seq, HR, B, sl, sh, sb, bw))
-    return FL_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
   maps[3] = maps[0];
   maps[4] = maps[1];
   maps[6] = maps[0];
   maps[7] = maps[0];
-  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, static_cast<int64_t>(B) * N_res, N_seq)) return FL_ERR_CUDA;
+  if (mask_bias && !encode_rows_f32(&maps[7], mask_bias, static_cast<int64_t>(B) * N_res, N_seq))
+    return cuda_fail("cuTensorMapEncodeTiled (mask bias)", cudaSuccess);
   const int grid = static_cast<int>(units < ds->sm_count ? units : ds->sm_count);
-  cudaError_t e = fl::launch_evo_col(d, maps, p, grid, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  return launched("Evoformer kernel launch", fl::launch_evo_col(d, maps, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,478 @@
+// Backward pass of the fused attention (dQ, dK, dV) for sm_103a.
+//
+// The derivative of softmax(score_mod(scale QK^T) + mask) V, recomputing P
+// from the forward's log-sum-exp instead of storing it (the same recompute
+// the fused forward's single pass makes possible; the Flashlight wiki
+// summary lists the training backward as future work, 局限与 Future Work):
+//
+//   P^T  = exp(T^T - LSE)          dV += P^T dO
+//   dP^T = V dO^T                  dS^T = P^T * (dP^T - D) * dT/dS
+//   dK  += dS^T Q                  dQ  += dS K        (D = rowsum(dO * O))
+//
+// One CTA owns one (batch, key/value head, 128-key tile) and walks every
+// query tile of every query head of its GQA group that sees those keys;
+// dK and dV stay in TMEM for the whole walk, and each query tile's dQ
+// contribution is added to an fp32 accumulator in global memory.  All five
+// products run on tcgen05 with accumulators in TMEM:
+//   S^T  = K Q^T   (A = K smem, B = Q smem)         TMEM [0,128)
+//   P^T  (bf16, written by the compute warps)        TMEM [128,192)
+//   dP^T = V dO^T  (A = V smem, B = dO smem)        TMEM [192,320)
+//   dS^T (bf16, over the first half of dP^T)         TMEM [192,256)
+//   dV  += P^T dO  (A = P^T TMEM, B = dO smem)      TMEM [320,320+D)
+//   dK  += dS^T Q  (A = dS^T TMEM, B = Q smem)      TMEM [320+D,320+2D)
+//   dQ   = dS K    (A = dS smem, M-major; B = K)    TMEM [320+2D,320+3D)
+// Warp roles (384 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-7
+// compute P and dS (one thread per key row), warps 8-11 add dQ into the
+// accumulator (one thread per query row).  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "bwd.h"
+#include "fused_attn.cuh"
+
+namespace fl {
+namespace {
+
+constexpr int kBwdThreads = 384;
+
+template <int D>
+struct BwdLayout {
+  static_assert(D == 32 || D == 64, "backward head dim");
+  static constexpr int ROWB = D * 2;
+  static constexpr int TILE = 128 * ROWB;              // one 128-row tile of K, V, Q or dO
+  static constexpr uint32_t SWZ = ROWB == 128 ? 2u : 4u;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;               // Q[2]
+  static constexpr int OFF_DO = 4 * TILE;              // dO[2]
+  static constexpr int OFF_DS = 6 * TILE;              // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
+  static constexpr int OFF_VEC = OFF_DS + 2 * 128 * 128;  // fp32 L2[2][128], Dv[2][128]
+  static constexpr int OFF_BAR = OFF_VEC + 4 * 128 * 4;
+  static constexpr int NBARS = 16;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static_assert(SMEM <= 227 * 1024, "backward shared memory");
+};
+
+// Queries that see key k form one interval [qlo, qhi] for every mask kind
+// (the mirror of row_bounds: the visible-key intervals of the rows are
+// non-decreasing in the row).
+__device__ __forceinline__ void col_bounds(const BwdParams& p, int b, int k, int& qlo, int& qhi) {
+  qlo = 0;
+  qhi = p.Lq - 1;
+  switch (p.mask_kind) {
+    case MASK_NONE: break;
+    case MASK_CAUSAL: qlo = k; break;
+    case MASK_WINDOW: qlo = k; qhi = k + p.window - 1; break;
+    case MASK_PREFIX: qlo = k < p.prefix ? 0 : k; break;
+    default: {
+      const int32_t* off = p.doc_offsets + static_cast<int64_t>(b) * (p.num_docs + 1);
+      int a = 0, z = p.num_docs - 1;
+      while (a < z) {
+        const int mid = (a + z + 1) >> 1;
+        if (__ldg(off + mid) <= k) a = mid; else z = mid - 1;
+      }
+      qlo = __ldg(off + a);
+      qhi = __ldg(off + a + 1) - 1;
+      if (p.doc_causal) qlo = k > qlo ? k : qlo;
+    }
+  }
+  qhi = qhi > p.Lq - 1 ? p.Lq - 1 : qhi;
+}
+
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmDv,
+                    const __grid_constant__ BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t kColS = 0, kColP = 128, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
+  extern __shared__ uint8_t bsm_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;    // [2]
+  uint64_t* q_empty = bars + 3;   // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* dp_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* ds_full = bars + 8;
+  uint64_t* dq_full = bars + 9;
+  uint64_t* dq_free = bars + 10;
+  uint64_t* done = bars + 11;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // L2[buf][128] then Dv[buf][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this CTA: (batch b, key/value head hkv, key tile jt)
+  const int jt = blockIdx.x % p.n_ktiles;
+  const int bh = blockIdx.x / p.n_ktiles;
+  const int hkv = bh % p.Hkv, b = bh / p.Hkv;
+  const int j0 = jt * 128;
+  const int group = p.Hq / p.Hkv;
+  // query tiles that see any key of the tile (intervals are monotone in k)
+  int qlo0, qhi0, qlo1, qhi1;
+  col_bounds(p, b, j0, qlo0, qhi0);
+  col_bounds(p, b, min(j0 + 127, p.Lk - 1), qlo1, qhi1);
+  const int it_lo = qlo0 / 128;
+  const int it_hi = qhi1 >= qlo0 ? qhi1 / 128 : it_lo - 1;
+  const int nq = it_hi - it_lo + 1;
+  const int n_tiles = nq > 0 ? nq * group : 0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&q_full[i], 1);
+      ptx::mbar_init(&q_empty[i], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(dq_full, 1);
+    ptx::mbar_init(dq_free, 4);
+    ptx::mbar_init(done, 1);
+    misc[1] = 0u;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&misc[0], 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const Ctl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), p.status, p.timeout_ns};
+  const uint64_t drain_ns = 50ull * 1000ull * 1000ull;
+
+  if (warp < 4) {
+    ptx::setmaxnreg_dec<kCtlRegs>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- TMA
+      const uint64_t pol_keep = ptx::policy_evict_last();
+      if (n_tiles > 0) {
+        ptx::mbar_arrive_expect_tx(kv_full, 2u * L::TILE);
+        ptx::tma_load_4d(smem + L::OFF_K, &tmK, kv_full, 0, j0, hkv, b, pol_keep);
+        ptx::tma_load_4d(smem + L::OFF_V, &tmV, kv_full, 0, j0, hkv, b, pol_keep);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
+        const int buf = n & 1;
+        if (!wait_bar(&q_empty[buf], ((n >> 1) & 1u) ^ 1u, ctl, 50)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(&q_full[buf], 2u * L::TILE + 2u * 512u);
+        ptx::tma_load_4d(smem + L::OFF_Q + buf * L::TILE, &tmQ, &q_full[buf], 0, i0, h, b, pol_keep);
+        ptx::tma_load_4d(smem + L::OFF_DO + buf * L::TILE, &tmDO, &q_full[buf], 0, i0, h, b, pol_keep);
+        const int row = b * p.Hq + h;
+        ptx::tma_load_2d(vec + buf * 128, &tmL2, &q_full[buf], i0, row, pol_keep);
+        ptx::tma_load_2d(vec + 256 + buf * 128, &tmDv, &q_full[buf], i0, row, pol_keep);
+        issued = n + 1;
+      }
+      if (*ctl.abort) {
+        if (n_tiles > 0) wait_drain(kv_full, 0u, drain_ns);
+        for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n) wait_drain(&q_full[n & 1], (n >> 1) & 1u, drain_ns);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      constexpr uint32_t ID_SS = ptx::idesc_bf16_f32(128, 128, false);        // S^T, dP^T
+      constexpr uint32_t ID_ACC = ptx::idesc_bf16_f32(128, D, true);          // dV, dK (B = dO / Q, N-major)
+      constexpr uint32_t ID_DQ = ptx::idesc_bf16_f32(128, D, true) | (1u << 15);  // dQ: A = dS, M-major
+      const uint32_t k_a = ptx::smem_u32(smem + L::OFF_K), v_a = ptx::smem_u32(smem + L::OFF_V);
+      const uint32_t ds_a = ptx::smem_u32(smem + L::OFF_DS);
+      bool ok = n_tiles == 0 || wait_bar(kv_full, 0u, ctl, 51);
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        const int buf = n & 1;
+        const uint32_t ph = n & 1;
+        if (!wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 52)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t q_a = ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE);
+        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + buf * L::TILE);
+        // S^T = K Q^T and dP^T = V dO^T (both K-major, k-steps of 16 channels)
+        const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::ROWB, L::SWZ), qb = ptx::smem_desc(q_a, 16, 8 * L::ROWB, L::SWZ);
+        const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::ROWB, L::SWZ), dob = ptx::smem_desc(do_a, 16, 8 * L::ROWB, L::SWZ);
+#pragma unroll
+        for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColS, ka + kb * 2, qb + kb * 2, ID_SS, kb > 0);
+        ptx::mma_commit(s_full);
+#pragma unroll
+        for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColDP, va + kb * 2, dob + kb * 2, ID_SS, kb > 0);
+        ptx::mma_commit(dp_full);
+        // dV += P^T dO (B = dO as [queries][D], N contiguous)
+        if (!wait_bar(p_full, ph, ctl, 53)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint64_t don = ptx::smem_desc(do_a, L::TILE, 8 * L::ROWB, L::SWZ);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          ptx::mma_ts(tmem + kColDV, tmem + kColP + kb * 8, don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
+        // dK += dS^T Q, then dQ = dS K once the previous dQ has been read
+        if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint64_t qn = ptx::smem_desc(q_a, L::TILE, 8 * L::ROWB, L::SWZ);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8, qn + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
+        if (!wait_bar(dq_free, ph ^ 1u, ctl, 55)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint64_t dsa = ptx::smem_desc(ds_a, 128 * 128, 1024, 2u);
+        const uint64_t kn = ptx::smem_desc(k_a, L::TILE, 8 * L::ROWB, L::SWZ);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          ptx::mma_ss(tmem + kColDQ, dsa + ((kb * 16 * 128) >> 4), kn + ((kb * 16 * L::ROWB) >> 4), ID_DQ, kb > 0);
+        ptx::mma_commit(dq_full);
+        ptx::mma_commit(&q_empty[buf]);
+      }
+      ptx::mma_commit(done);
+      wait_drain(done, 0u, drain_ns);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem, 512);
+    }
+  } else if (warp < 8) {
+    // -------------------------------------------------- P and dS (key rows)
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;          // key row of the tile
+    const int kg = j0 + r;                   // key index
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    int cqlo, cqhi;
+    col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
+    if (kg >= p.Lk) { cqlo = 1; cqhi = 0; }  // keys past the end see nothing
+    const float scale_log2 = p.scale * kLog2e;
+    bool ok = true;
+    for (int n = 0; n < n_tiles && ok; ++n) {
+      const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
+      const int buf = n & 1;
+      const uint32_t ph = n & 1;
+      const float* l2 = vec + buf * 128;
+      const float* dvec = vec + 256 + buf * 128;
+      if (!__all_sync(0xffffffffu, wait_bar(s_full, ph, ctl, 60))) { ok = false; break; }
+      // this tile's LSE and D rows came with Q (TMA); observe that barrier too
+      if (!__all_sync(0xffffffffu, wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 64))) { ok = false; break; }
+      ptx::tc_fence_after();
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) ptx::tmem_ld32f(tl + kColS + c, &x[c]);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) ptx::reg_fence32f(&x[c]);
+      const float slope2 = SCORE == SCORE_ALIBI ? __ldg(p.slopes + h) * kLog2e : 0.f;
+      const bool any_vis = __any_sync(0xffffffffu, cqlo <= i0 + 127 && cqhi >= i0);
+      // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float t;
+        if (SCORE == SCORE_SOFTCAP) {
+          const float kcap = p.softcap * kLog2e;
+          const float ez = ptx::ex2(x[c] * (2.0f * scale_log2 / p.softcap));
+          t = fmaf(-2.0f * kcap, ptx::rcp(1.0f + ez), kcap);
+        } else if (SCORE == SCORE_ALIBI) {
+          t = fmaf(x[c], scale_log2, slope2 * static_cast<float>(kg - (i0 + c)));
+        } else {
+          t = x[c] * scale_log2;
+        }
+        const int q = i0 + c;
+        const bool vis = any_vis && q >= cqlo && q <= cqhi;
+        x[c] = vis ? ptx::ex2(t - l2[c]) : 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = ptx::pack_bf16x2(x[c + 2 * e], x[c + 2 * e + 1]);
+        ptx::tmem_st16(tl + kColP + c / 2, pk);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_full);
+      // dS^T = P^T (dP^T - D_q) (* 1 - tanh^2 for softcap), 32 columns at a time
+      if (!__all_sync(0xffffffffu, wait_bar(dp_full, ph, ctl, 61))) { ok = false; break; }
+      // the previous dQ product must have read the dS tile in shared memory
+      if (n > 0 && !__all_sync(0xffffffffu, wait_bar(dq_full, ph ^ 1u, ctl, 62))) { ok = false; break; }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        float dpv[32];
+        ptx::tmem_ld32f(tl + kColDP + c, dpv);
+        float sv[32];
+        if (SCORE == SCORE_SOFTCAP) ptx::tmem_ld32f(tl + kColS + c, sv);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32f(dpv);
+        if (SCORE == SCORE_SOFTCAP) ptx::reg_fence32f(sv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float d0 = x[c + e] * (dpv[e] - dvec[c + e]);
+          float d1 = x[c + e + 1] * (dpv[e + 1] - dvec[c + e + 1]);
+          if (SCORE == SCORE_SOFTCAP) {
+            const float th0 = tanhf(sv[e] * p.scale / p.softcap), th1 = tanhf(sv[e + 1] * p.scale / p.softcap);
+            d0 *= 1.0f - th0 * th0;
+            d1 *= 1.0f - th1 * th1;
+          }
+          pk[e / 2] = ptx::pack_bf16x2(d0, d1);
+        }
+        // dS^T over the first half of the dP^T columns (already read) ...
+        ptx::tmem_st16(tl + kColDP + c / 2, pk);
+        // ... and dS into shared memory: row r (key) of two [128][64] boxes,
+        // 16-byte chunks at the 128-byte swizzle positions
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int qc = c + 8 * w;                      // first query column of this chunk
+          const int bx = qc >> 6, chunk = (qc & 63) >> 3;
+          *reinterpret_cast<uint4*>(smem + L::OFF_DS + bx * 128 * 128 + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ds_full);
+    }
+    // dK, dV of this thread's key row, once every product is done (the
+    // TMEM loads are warp-wide; only the stores depend on the row)
+    if (ok && __all_sync(0xffffffffu, wait_bar(done, 0u, ctl, 63))) {
+      ptx::tc_fence_after();
+      const int64_t roff = ((static_cast<int64_t>(b) * p.Hkv + hkv) * p.Lk + kg) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float a[D];
+#pragma unroll
+        for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + (which ? kColDK : kColDV) + c, &a[c]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
+        const float f = (which && n_tiles > 0) ? p.scale : 1.0f;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + roff);
+        if (kg >= p.Lk) continue;
+#pragma unroll
+        for (int c = 0; c < D; c += 8) {
+          const bool z = n_tiles == 0;
+          dst[c / 8] = make_uint4(ptx::pack_bf16x2(z ? 0.f : a[c] * f, z ? 0.f : a[c + 1] * f),
+                                  ptx::pack_bf16x2(z ? 0.f : a[c + 2] * f, z ? 0.f : a[c + 3] * f),
+                                  ptx::pack_bf16x2(z ? 0.f : a[c + 4] * f, z ? 0.f : a[c + 5] * f),
+                                  ptx::pack_bf16x2(z ? 0.f : a[c + 6] * f, z ? 0.f : a[c + 7] * f));
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+  } else {
+    // ------------------------------------------- dQ accumulation (query rows)
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;          // query row of the tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    bool ok = true;
+    for (int n = 0; n < n_tiles && ok; ++n) {
+      const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
+      if (!__all_sync(0xffffffffu, wait_bar(dq_full, n & 1u, ctl, 70))) { ok = false; break; }
+      ptx::tc_fence_after();
+      float a[D];
+#pragma unroll
+      for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + kColDQ + c, &a[c]);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(dq_free);
+      if (i0 + r < p.Lq) {
+        float* dst = p.dq_acc + ((static_cast<int64_t>(b) * p.Hq + h) * p.Lq + i0 + r) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 4)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c), "f"(a[c]), "f"(a[c + 1]),
+                       "f"(a[c + 2]), "f"(a[c + 3])
+                       : "memory");
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
+}
+
+// D_i = sum_c dO_ic O_ic, L2_i = LSE_i log2(e) (a row that saw no key:
+// +inf, so that its P is 0), and the dQ accumulator zeroed; one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.rows) return;
+  constexpr int PER = D / 32;
+  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + row * D + lane * PER;
+  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * PER;
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < PER; ++c) s = fmaf(__bfloat162float(o[c]), __bfloat162float(g[c]), s);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  float* acc = p.dq_acc + row * D + lane * PER;
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+  if (lane == 0) {
+    p.dvec[row] = s;
+    const float l = p.lse[row];
+    p.l2[row] = l == -CUDART_INF_F ? CUDART_INF_F : l * kLog2e;
+  }
+}
+
+// dQ = scale * accumulator, rounded to bf16.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constant__ BwdParams p) {
+  const int64_t e = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
+  if (e >= p.rows * D) return;
+  reinterpret_cast<__nv_bfloat162*>(p.dq)[e / 2] =
+      __floats2bfloat162_rn(p.dq_acc[e] * p.scale, p.dq_acc[e + 1] * p.scale);
+}
+
+template <int D, int SCORE>
+cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+  auto kern = attn_bwd_kernel<D, SCORE>;
+  constexpr int smem = BwdLayout<D>::SMEM;
+  static const cudaError_t checked = [&]() {
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, kern);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs != kLaunchRegs) return cudaErrorInvalidDeviceFunction;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  }();
+  if (checked != cudaSuccess) return checked;
+  const int rgrid = static_cast<int>((p.rows + 7) / 8);
+  attn_bwd_pre_kernel<D><<<rgrid, 256, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kern<<<p.B * p.Hkv * p.n_ktiles, kBwdThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int pgrid = static_cast<int>((p.rows * D / 2 + 255) / 256);
+  attn_bwd_post_kernel<D><<<pgrid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_d(int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+  switch (score_mod) {
+    case SCORE_NONE: return launch_bwd_ds<D, SCORE_NONE>(maps, p, s);
+    case SCORE_ALIBI: return launch_bwd_ds<D, SCORE_ALIBI>(maps, p, s);
+    default: return launch_bwd_ds<D, SCORE_SOFTCAP>(maps, p, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+  return d == 32 ? launch_bwd_d<32>(score_mod, maps, p, s) : launch_bwd_d<64>(score_mod, maps, p, s);
+}
+
+}  // namespace fl

@@ -1,0 +1,35 @@
+// Backward pass of the fused attention: parameters shared by the host
+// launcher and the kernels (internal header).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fl {
+
+struct BwdParams {
+  const void* out;        // bf16 [B, Hq, Lq, D] forward output
+  const void* dout;       // bf16 [B, Hq, Lq, D] gradient of the output
+  const float* lse;       // fp32 [B, Hq, Lq] forward log-sum-exp (natural log)
+  void* dq;               // bf16 [B, Hq, Lq, D]
+  void* dk;               // bf16 [B, Hkv, Lk, D]
+  void* dv;               // bf16 [B, Hkv, Lk, D]
+  float* dq_acc;          // fp32 [B, Hq, Lq, D] workspace
+  float* dvec;            // fp32 [B, Hq, Lq] workspace: rowsum(dO * O)
+  float* l2;              // fp32 [B, Hq, Lq] workspace: LSE * log2(e)
+  const float* slopes;    // ALiBi slopes [Hq]
+  const int32_t* doc_offsets;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int B, Hq, Hkv, Lq, Lk;
+  int n_ktiles;           // ceil(Lk / 128)
+  int64_t rows;           // B * Hq * Lq
+  float scale, softcap;
+  int mask_kind, doc_causal, window, prefix, num_docs;
+};
+
+cudaError_t launch_bwd(int d, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
+
+}  // namespace fl

@@ -45,6 +45,9 @@ NoAllocDevice g_na_dev[kMaxDevices];
 fl_status na_setup(NoAllocDevice** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FL_ERR_CUDA;
+  // the device's primary context current on this thread (the tensor-map
+  // encoder is a driver call)
+  if (cudaSetDevice(dev) != cudaSuccess) return FL_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_na_mutex);
   NoAllocDevice& d = g_na_dev[dev];
   if (!d.ready) {

@@ -72,6 +72,18 @@ def attn_counts(B, Hq, Hkv, L, d, dv=None, *, mask="none", window=None, prefix=N
     return tile_flops, exact_flops, bytes_
 
 
+def bwd_counts(B, Hq, Hkv, L, d, *, mask="none", window=None, prefix=None, doc_offsets=None,
+               doc_causal=False):
+    """Backward pass: five products per visible pair (S = QK^T and dP = dO V^T
+    recomputed, dV, dK, dQ), 2*d FLOPs each; bytes read q, k, v, out, dout,
+    lse and written dq, dk, dv once."""
+    tf, ef, _ = attn_counts(B, Hq, Hkv, L, d, mask=mask, window=window, prefix=prefix,
+                            doc_offsets=doc_offsets, doc_causal=doc_causal)
+    f = 10 / 4  # 10 d per pair against the forward's 4 d
+    bytes_ = 2 * (3 * B * Hq * L * d + 2 * B * Hkv * L * d) + 4 * B * Hq * L + 2 * (B * Hq * L * d + 2 * B * Hkv * L * d)
+    return int(tf * f), int(ef * f), bytes_
+
+
 def diff_counts(B, H, L, d=64, dv=128, causal=True):
     lo, hi = row_intervals("causal" if causal else "none", L)
     tiles, pairs = visible_tiles(lo, hi, L), visible_pairs(lo, hi)

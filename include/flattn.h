@@ -205,6 +205,30 @@ FL_API fl_status fl_attn_decode_fwd(const void* q, const void* k_cache, const vo
 FL_API size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc);
 
 /*
+ * Backward pass of fl_attn_fwd (the Flashlight wiki summary lists the
+ * training backward under 局限与 Future Work; the definition is the plain
+ * derivative of the forward): given dout = dL/dout, returns
+ *   dv = P^T dout,  dq = scale dS K,  dk = scale dS^T q,
+ *   dS = P * (dout v^T - rowsum(dout * out)) * dT/dS
+ * with P recomputed from the forward's lse (dT/dS = 1 - tanh(s/cap)^2 for
+ * softcap, else 1); GQA sums dk, dv over each group's query heads.
+ *   q, out, dout, dq : bf16 [B, Hq, Lq, d] contiguous
+ *   k, v, dk, dv     : bf16 [B, Hkv, Lk, d] contiguous
+ *   lse              : fp32 [B, Hq, Lq], the forward's (natural log)
+ *   workspace        : caller-owned device buffer of at least
+ *                      fl_attn_bwd_workspace_size(desc) bytes (16-byte
+ *                      aligned): an fp32 dq accumulator and two per-row vectors
+ * desc: the forward's descriptor; d == dv in {32, 64}, Lq a multiple of 4,
+ * strides zero.  Masks, ALiBi and softcap as in fl_attn_fwd.
+ */
+FL_API fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                             size_t workspace_bytes, const fl_attn_desc* desc);
+
+/* Workspace bytes fl_attn_bwd needs for `desc` (0 on an invalid descriptor). */
+FL_API size_t fl_attn_bwd_workspace_size(const fl_attn_desc* desc);
+
+/*
  * Allocation-free variant of fl_attn_fwd (no counterpart in the paper; it is
  * a property of this library's interface).  For callers that cannot let a
  * library call cudaMalloc: processes whose device memory all comes from
@@ -234,6 +258,10 @@ FL_API fl_status fl_attn_fwd_noalloc(const void* q, const void* k, const void* v
 /* Synchronise `stream`, then return and clear the device status word of the
    current device (FL_OK, or FL_ERR_TIMEOUT if a kernel gave up waiting). */
 FL_API fl_status fl_sync_status(void* stream);
+
+/* What the last call on this thread that returned FL_ERR_CUDA failed on
+   (the CUDA call or step and CUDA's message); "" if none has. */
+FL_API const char* fl_last_error_detail(void);
 
 /* Static description of a status code. */
 FL_API const char* fl_status_string(fl_status status);

@@ -171,6 +171,7 @@ def test_decode_split_arithmetic():
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_cuda_error(L):
     assert _attn(L, _desc()) == _lib.FL_ERR_CUDA
+    assert L.fl_last_error_detail().decode().startswith("cudaGetDevice")
     assert L.fl_sync_status(None) == _lib.FL_ERR_CUDA
 
 
