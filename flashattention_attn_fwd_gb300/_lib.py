@@ -41,6 +41,7 @@ EXPORTS = (
     "fl_attn_bwd",
     "fl_attn_bwd_workspace_size",
     "fl_last_error_detail",
+    "fl_attn_schedule",
 )
 
 
@@ -107,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.fl_attn_bwd_workspace_size.restype = ctypes.c_size_t
         L.fl_sync_status.argtypes = [vp]
         L.fl_sync_status.restype = i32
+        L.fl_attn_schedule.argtypes = [ctypes.POINTER(AttnDesc), vp, ctypes.POINTER(ctypes.c_int64)]
+        L.fl_attn_schedule.restype = i32
         L.fl_last_error_detail.argtypes = []
         L.fl_last_error_detail.restype = ctypes.c_char_p
         L.fl_status_string.argtypes = [i32]

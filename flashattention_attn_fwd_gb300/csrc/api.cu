@@ -12,6 +12,7 @@
 #include "bwd.h"
 #include "decode.h"
 #include "flattn.h"
+#include "fused_attn.cuh"
 #include "host.h"
 #include "kernels.h"
 #include "params.h"
@@ -203,6 +204,38 @@ cudaError_t launch_attn(int d, int dv, int score_mod, const CUtensorMap* maps, c
   return cudaErrorInvalidValue;
 }
 
+// Kernel parameters of fl_attn_fwd for a validated descriptor (out strides
+// `so`, status words `status`): problem, variant, schedule.
+fl_status fill_attn_params(const fl_attn_desc& d, const Strides& so, uint32_t* status, KParams* p) {
+  p->B = d.B; p->Hq = d.Hq; p->Hkv = d.Hkv; p->Lq = d.Lq; p->Lk = d.Lk;
+  p->group = d.Hq / d.Hkv;
+  p->n_qtiles = (d.Lq + fl::kBlockM - 1) / fl::kBlockM;
+  const float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
+  p->scale = scale;
+  p->scale_log2 = scale * static_cast<float>(kLog2e);
+  p->mask_kind = d.mask_kind; p->doc_causal = d.doc_causal ? 1 : 0;
+  p->window = d.window; p->prefix = d.prefix_len;
+  p->doc_offsets = d.doc_offsets; p->num_docs = d.num_docs;
+  p->slopes = d.alibi_slopes; p->softcap = d.softcap;
+  if (d.score_mod == FL_SCORE_SOFTCAP) softcap_coefficients(*p, scale, d.softcap);
+  p->o_sb = so.b; p->o_sh = so.h; p->o_sl = so.l;
+  p->status = status;
+  p->timeout_ns = wait_ns(d.wait_limit_ms);
+  p->dbg_skip_tile = (d.debug_flags & FL_DEBUG_SKIP_KV_LOAD) ? (d.debug_arg < 0 ? 0 : d.debug_arg) : -1;
+  int64_t units;
+  if (p->group == 1) {
+    p->slot_mode = fl::SLOT_ROWS;
+    units = static_cast<int64_t>(d.B) * d.Hq * ((p->n_qtiles + 1) / 2);
+  } else {
+    p->slot_mode = fl::SLOT_HEADS;
+    p->pairs_per_group = (p->group + 1) / 2;
+    units = static_cast<int64_t>(d.B) * d.Hkv * p->pairs_per_group * p->n_qtiles;
+  }
+  if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
+  p->num_units = static_cast<int>(units);
+  return FL_OK;
+}
+
 }  // namespace
 
 namespace fl {
@@ -247,33 +280,11 @@ fl_status attn_fwd_launch(const void* q, const void* k, const void* v, void* out
   resolve_strides(d.o_strides, d.Hq, d.Lq, d.dv, &so);
 
   KParams p{};
-  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.Lq = d.Lq; p.Lk = d.Lk;
-  p.group = d.Hq / d.Hkv;
-  p.n_qtiles = (d.Lq + fl::kBlockM - 1) / fl::kBlockM;
-  const float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
-  p.scale = scale;
-  p.scale_log2 = scale * static_cast<float>(kLog2e);
-  p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
-  p.window = d.window; p.prefix = d.prefix_len;
-  p.doc_offsets = d.doc_offsets; p.num_docs = d.num_docs;
-  p.slopes = d.alibi_slopes; p.softcap = d.softcap;
-  if (d.score_mod == FL_SCORE_SOFTCAP) softcap_coefficients(p, scale, d.softcap);
-  p.out = out; p.o_sb = so.b; p.o_sh = so.h; p.o_sl = so.l;
+  const fl_status fs = fill_attn_params(d, so, status, &p);
+  if (fs != FL_OK) return fs;
+  p.out = out;
   p.lse = lse;
-  p.status = status;
-  p.timeout_ns = wait_ns(d.wait_limit_ms);
-  p.dbg_skip_tile = (d.debug_flags & FL_DEBUG_SKIP_KV_LOAD) ? (d.debug_arg < 0 ? 0 : d.debug_arg) : -1;
-  int64_t units;
-  if (p.group == 1) {
-    p.slot_mode = fl::SLOT_ROWS;
-    units = static_cast<int64_t>(d.B) * d.Hq * ((p.n_qtiles + 1) / 2);
-  } else {
-    p.slot_mode = fl::SLOT_HEADS;
-    p.pairs_per_group = (p.group + 1) / 2;
-    units = static_cast<int64_t>(d.B) * d.Hkv * p.pairs_per_group * p.n_qtiles;
-  }
-  if (units > 0x7fffffff) return FL_ERR_UNSUPPORTED;
-  p.num_units = static_cast<int>(units);
+  const int64_t units = p.num_units;
 
   CUtensorMap maps[8];
   const int bq = box_width(d.d), bv = box_width(d.dv);
@@ -337,6 +348,41 @@ fl_status fl_sync_status(void* stream) {
   const cudaError_t me = cudaMemset(ds->status, 0, 2 * sizeof(uint32_t));
   if (me != cudaSuccess) return cuda_fail("cudaMemset (status word)", me);
   return (h[0] & 1u) ? FL_ERR_TIMEOUT : FL_ERR_DEVICE_BOUNDS;
+}
+
+fl_status fl_attn_schedule(const fl_attn_desc* desc, const int32_t* doc_offsets_host, int64_t* tiles) {
+  if (!desc || !tiles) return FL_ERR_INVALID_ARG;
+  fl_attn_desc d = *desc;
+  if (d.mask_kind == FL_MASK_DOCUMENT) {
+    if (!doc_offsets_host) return FL_ERR_INVALID_ARG;
+    d.doc_offsets = doc_offsets_host;
+  }
+  static const int64_t kFake = 0x10000;  // only validated, never dereferenced
+  const void* f = reinterpret_cast<const void*>(kFake);
+  if (d.score_mod == FL_SCORE_ALIBI && !d.alibi_slopes) d.alibi_slopes = static_cast<const float*>(f);
+  const fl_status chk = fl::attn_fwd_check(f, f, f, const_cast<void*>(f), nullptr, &d);
+  if (chk != FL_OK) return chk;
+  Strides so;
+  resolve_strides(d.o_strides, d.Hq, d.Lq, d.dv, &so);
+  KParams p{};
+  const fl_status fs = fill_attn_params(d, so, nullptr, &p);
+  if (fs != FL_OK) return fs;
+  const bool per_slot = d.dv <= 64;  // one MMA thread per slot: per-slot key ranges
+  int64_t own = 0, all = 0;
+  for (int u = 0; u < p.num_units; ++u) {
+    const fl::Unit U = fl::decode_unit<fl::KIND_ATTN>(p, u, per_slot);
+    for (int s = 0; s < 2; ++s) {
+      const int64_t n = U.hi[s] - U.lo[s] + 1;
+      all += n;
+      if (U.valid[s] && U.row0[s] < p.Lq && !(p.slot_mode == fl::SLOT_HEADS && s == 1 && U.hq[1] == U.hq[0]))
+        own += n;
+    }
+  }
+  const int64_t nq = (d.Lq + 127) / 128, nk = (d.Lk + 127) / 128;
+  tiles[0] = own;
+  tiles[1] = all;
+  tiles[2] = static_cast<int64_t>(d.B) * d.Hq * nq * nk;
+  return FL_OK;
 }
 
 fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,

@@ -196,8 +196,18 @@ struct Unit {
 };
 static_assert(sizeof(Unit) <= 128, "unit ring entry");
 
+// Reads of the document offsets: through the read-only cache on the device,
+// plainly on the host (the host-side schedule query gets host offsets).
+__host__ __device__ __forceinline__ int32_t load_offset(const int32_t* x) {
+#ifdef __CUDA_ARCH__
+  return __ldg(x);
+#else
+  return *x;
+#endif
+}
+
 // Visible keys of query row i form one interval [lo, hi] for every mask kind.
-__device__ __forceinline__ void row_bounds(const KParams& p, int b, int i, int& lo, int& hi) {
+__host__ __device__ __forceinline__ void row_bounds(const KParams& p, int b, int i, int& lo, int& hi) {
   switch (p.mask_kind) {
     case MASK_NONE: lo = 0; hi = p.Lk - 1; break;
     case MASK_CAUSAL: lo = 0; hi = i; break;
@@ -208,10 +218,10 @@ __device__ __forceinline__ void row_bounds(const KParams& p, int b, int i, int& 
       int a = 0, z = p.num_docs - 1;
       while (a < z) {
         const int mid = (a + z + 1) >> 1;
-        if (__ldg(off + mid) <= i) a = mid; else z = mid - 1;
+        if (load_offset(off + mid) <= i) a = mid; else z = mid - 1;
       }
-      lo = __ldg(off + a);
-      hi = p.doc_causal ? i : __ldg(off + a + 1) - 1;
+      lo = load_offset(off + a);
+      hi = p.doc_causal ? i : load_offset(off + a + 1) - 1;
     }
   }
   lo = lo < 0 ? 0 : lo;
@@ -237,7 +247,7 @@ __device__ __forceinline__ Sched make_sched(const KParams& p) {
 }
 
 template <int KIND>
-__device__ __forceinline__ Unit decode_unit(const KParams& p, int u, bool per_slot) {
+__host__ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, bool per_slot) {
   Unit U;
   U.pb_b = 0;
   U.pb_h = 0;

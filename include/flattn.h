@@ -124,6 +124,21 @@ FL_API fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* 
                       const fl_attn_desc* desc);
 
 /*
+ * Block-sparse schedule of fl_attn_fwd for `desc`, without running it (the
+ * Flashlight wiki summary's open question 设计取舍 / 局限与 Future Work: whether
+ * block_mask sparsity can be handled by analysing the mask at compile time
+ * instead of building a block mask at run time).  The kernel derives, from
+ * the descriptor alone, the key tiles each 128-row query tile visits; this
+ * call walks the same schedule on the host and reports
+ *   tiles[0]  (query tile, key tile) pairs computed for rows that exist,
+ *   tiles[1]  the same including the padding slot of an odd tile count,
+ *   tiles[2]  the dense count B * Hq * ceil(Lq/128) * ceil(Lk/128).
+ * doc_offsets_host: host copy of the document offsets (DOCUMENT only).
+ * Pointers in desc other than doc offsets are not read.
+ */
+FL_API fl_status fl_attn_schedule(const fl_attn_desc* desc, const int32_t* doc_offsets_host, int64_t* tiles);
+
+/*
  * Differential attention (the Flashlight pages, Problem Statement and Results,
  * name it; definition is this library's reading):
  *   out = softmax(scale Q1 K1^T) V - lambda * softmax(scale Q2 K2^T) V

@@ -262,6 +262,27 @@ def test_skipped_tile_load_times_out_then_recovers():
     check(out, ro, lse, rl)
 
 
+@pytest.mark.parametrize("L", [1, 17, 129, 255, 300])
+def test_output_guard_regions_untouched(L):
+    """out and lse placed inside larger buffers whose guard regions hold a
+    sentinel; ragged shapes must write exactly their own elements."""
+    B, H, d = 1, 2, 64
+    q, k, v = synth.attn_inputs(B, H, H, L, d, seed=L)
+    pad = 4096  # elements of guard on each side (a multiple of 8: 16-byte aligned)
+    n_out, n_lse = B * H * L * d, B * H * L
+    obuf = torch.full((pad + n_out + pad,), -7.0, dtype=torch.bfloat16, device=DEV)
+    lbuf = torch.full((pad + n_lse + pad,), 12345.0, dtype=torch.float32, device=DEV)
+    out = obuf[pad:pad + n_out].view(B, H, L, d)
+    lse = lbuf[pad:pad + n_lse].view(B, H, L)
+    attn_fwd(*_gpu(q, k, v), mask="causal", out=out, lse=lse)
+    sync_status()
+    ob, lb = obuf.cpu(), lbuf.cpu()
+    assert torch.all(ob[:pad] == -7.0) and torch.all(ob[pad + n_out:] == -7.0)
+    assert torch.all(lb[:pad] == 12345.0) and torch.all(lb[pad + n_lse:] == 12345.0)
+    ro, rl = oracle.attention(q, k, v, mask="causal")
+    check(out, ro, lse, rl)
+
+
 def test_softcap_both_tanh_paths():
     """Scores inside the polynomial range (|s*scale/cap| <= 0.5) take the FMA
     path, a large-score tile takes the exact MUFU path; both must match."""

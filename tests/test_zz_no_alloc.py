@@ -18,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from flashattention_attn_fwd_gb300 import _lib, synth
 
 ATOL, RTOL, LSE_ATOL = 2e-2, 1e-2, 1e-3
@@ -80,3 +81,49 @@ def test_noalloc_matches_fl_attn_fwd_on_two_calls_in_a_row():
         rel = float(np.linalg.norm(g - r) / np.linalg.norm(r))
         assert mae <= ATOL and rel <= RTOL, (mae, rel)
         assert float((lse - ref_l).abs().max()) <= LSE_ATOL
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle():
+    """The allocation-free path checked against the fp64 oracle directly."""
+    L = _lib.lib()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for (B, Hq, Hkv, S, d), kw, okw in (((1, 4, 4, 300, 64), dict(mask_kind=_lib.MASKS["window"], window=90),
+                                         dict(mask="window", window=90)),
+                                        ((2, 8, 2, 260, 32), dict(mask_kind=_lib.MASKS["causal"]), dict(mask="causal"))):
+        q, k, v = synth.attn_inputs(B, Hq, Hkv, S, d, seed=S + d)
+        out, lse = _run(L.fl_attn_fwd_noalloc, q.to(dev), k.to(dev), v.to(dev), _desc(B, Hq, Hkv, S, d, stream, **kw))
+        assert L.fl_attn_fwd_noalloc(0, 0, 0, 0, 0, ctypes.byref(_desc(B, Hq, Hkv, S, d, stream))) == _lib.FL_OK
+        ro, rl = oracle.attention(q, k, v, **okw)
+        g = out.float().cpu().numpy()
+        assert np.abs(g - ro).max() <= ATOL and np.linalg.norm(g - ro) / np.linalg.norm(ro) <= RTOL
+        assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_ATOL
+
+
+@pytest.mark.gpu
+def test_noalloc_timeout_is_recorded_in_its_own_array_and_cleared():
+    """A pipeline wait that runs out (block 0 never loads one key tile, 20 ms
+    limit) is recorded in the allocation-free path's own status words: the
+    query reports FL_ERR_TIMEOUT once and clears it, fl_sync_status's word is
+    untouched, and the next call is correct."""
+    L = _lib.lib()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    q, k, v = synth.attn_inputs(1, 2, 2, 512, 64, seed=1)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    bad = _desc(1, 2, 2, 512, 64, stream, debug_flags=_lib.FL_DEBUG_SKIP_KV_LOAD, debug_arg=1, wait_limit_ms=20)
+    out = torch.empty_like(qd)
+    lse = torch.empty(1, 2, 512, device=dev)
+    assert L.fl_attn_fwd_noalloc(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 ctypes.byref(bad)) == _lib.FL_OK
+    query = _desc(1, 2, 2, 512, 64, stream)
+    assert L.fl_attn_fwd_noalloc(0, 0, 0, 0, 0, ctypes.byref(query)) == _lib.FL_ERR_TIMEOUT
+    assert L.fl_attn_fwd_noalloc(0, 0, 0, 0, 0, ctypes.byref(query)) == _lib.FL_OK
+    assert L.fl_sync_status(stream) == _lib.FL_OK
+    out, lse = _run(L.fl_attn_fwd_noalloc, qd, kd, vd, _desc(1, 2, 2, 512, 64, stream))
+    assert L.fl_attn_fwd_noalloc(0, 0, 0, 0, 0, ctypes.byref(query)) == _lib.FL_OK
+    ro, rl = oracle.attention(q, k, v)
+    g = out.float().cpu().numpy()
+    assert np.abs(g - ro).max() <= ATOL and np.linalg.norm(g - ro) / np.linalg.norm(ro) <= RTOL
+    assert np.abs(lse.cpu().numpy() - rl).max() <= LSE_ATOL
