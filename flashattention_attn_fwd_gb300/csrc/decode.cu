@@ -171,24 +171,35 @@ __global__ void __launch_bounds__(kDecThreads, MR <= 16 ? 2 : 1)
       const int jg = j0 + j;
 #pragma unroll 1
       for (int m0 = mhalf; m0 < M; m0 += 2 * 4) {
-        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+        // two packed accumulators per row: four independent FMA chains per
+        // 8-channel chunk and row
+        float2 acc2[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc2[r][0] = acc2[r][1] = make_float2(0.f, 0.f);
+#pragma unroll 2
         for (int c = 0; c < D / 8; ++c) {
           const int bx = c >> 3, cq = c & 7;
           const uint4 kw = *reinterpret_cast<const uint4*>(ks + bx * kDecTileN * 128 + j * 128 + ((cq ^ (j & 7)) << 4));
-          float kf[8];
-          bf16x8_to_f32(kw, kf);
+          const float2 k01 = make_float2(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xffff0000u));
+          const float2 k23 = make_float2(__uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xffff0000u));
+          const float2 k45 = make_float2(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xffff0000u));
+          const float2 k67 = make_float2(__uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xffff0000u));
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int m = m0 + 2 * r;
             if (m < M) {
               const float4 qa = *reinterpret_cast<const float4*>(qs + m * D + 8 * c);
               const float4 qb = *reinterpret_cast<const float4*>(qs + m * D + 8 * c + 4);
-              sacc[r] = fmaf(qa.x, kf[0], fmaf(qa.y, kf[1], fmaf(qa.z, kf[2], fmaf(qa.w, kf[3], sacc[r]))));
-              sacc[r] = fmaf(qb.x, kf[4], fmaf(qb.y, kf[5], fmaf(qb.z, kf[6], fmaf(qb.w, kf[7], sacc[r]))));
+              acc2[r][0] = ptx::fma2(make_float2(qa.x, qa.y), k01, acc2[r][0]);
+              acc2[r][1] = ptx::fma2(make_float2(qa.z, qa.w), k23, acc2[r][1]);
+              acc2[r][0] = ptx::fma2(make_float2(qb.x, qb.y), k45, acc2[r][0]);
+              acc2[r][1] = ptx::fma2(make_float2(qb.z, qb.w), k67, acc2[r][1]);
             }
           }
         }
+        float sacc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sacc[r] = (acc2[r][0].x + acc2[r][0].y) + (acc2[r][1].x + acc2[r][1].y);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int m = m0 + 2 * r;
@@ -254,12 +265,12 @@ __global__ void __launch_bounds__(kDecThreads, MR <= 16 ? 2 : 1)
         const uint32_t vw = *reinterpret_cast<const uint32_t*>(vs + bx * kDecTileN * 128 + j * 128 +
                                                               ((cq ^ (j & 7)) << 4) + cw);
         const float v0 = __uint_as_float(vw << 16), v1 = __uint_as_float(vw & 0xffff0000u);
+        const float2 v01 = make_float2(v0, v1);
 #pragma unroll
         for (int m = 0; m < MR; ++m) {
           if (m < M) {
             const float pj = ps[m * kDecTileN + j];
-            acc[m].x = fmaf(pj, v0, acc[m].x);
-            acc[m].y = fmaf(pj, v1, acc[m].y);
+            acc[m] = ptx::fma2(make_float2(pj, pj), v01, acc[m]);
           }
         }
       }

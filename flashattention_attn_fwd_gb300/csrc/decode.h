@@ -29,11 +29,13 @@ struct DecodeParams {
   int score_mod, causal;
 };
 
-// Number of key splits and keys per split for a problem on `sm_count` SMs.
+// Number of key splits and keys per split for a problem on `sm_count` SMs:
+// enough CTAs for many waves (cache lengths differ per sequence, and a split
+// past a sequence's length has no work), whole 128-key tiles per split.
 inline void decode_split(int B, int Hkv, int Lmax, int sm_count, int* n_split, int* chunk) {
   const int tiles = (Lmax + 127) / 128;
   const int heads = B * Hkv;
-  int ns = (2 * sm_count + heads - 1) / heads;
+  int ns = (16 * sm_count + heads - 1) / heads;
   ns = ns < 1 ? 1 : (ns > tiles ? tiles : ns);
   const int tiles_per = (tiles + ns - 1) / ns;
   *chunk = tiles_per * 128;

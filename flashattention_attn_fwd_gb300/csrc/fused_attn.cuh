@@ -150,7 +150,9 @@ struct Layout {
   static constexpr int STAGE_BYTES = NK * K_BYTES + NV * V_BYTES + PB_BYTES + MB_BYTES;
   // barriers, misc words, the differential-attention exchange, the unit ring
   static constexpr int UNIT_BYTES = 128;
-  static constexpr int FIXED_BYTES = 64 * 8 + 64 + 2 * kBlockM * 4 + 4 * UNIT_BYTES + 8 * kBlockM * 4 + 4 * kBlockM * 4;
+  static constexpr int XCH_BYTES = KIND == KIND_DIFF ? 2 * kBlockM * 4 : 0;     // differential: row sums
+  static constexpr int XM_BYTES = kRowSplit == 2 ? 12 * kBlockM * 4 : 0;         // two threads per row
+  static constexpr int FIXED_BYTES = 64 * 8 + 64 + XCH_BYTES + 4 * UNIT_BYTES + XM_BYTES;
   static constexpr int BUDGET = 227 * 1024 - 1024 - FIXED_BYTES;
   // Q is double-buffered (the next unit's Q loads while this one runs) when
   // that still leaves room for two stages.
@@ -171,10 +173,10 @@ struct Layout {
   static_assert(NBARS <= 64, "barrier area");
   static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int OFF_XCH = OFF_MISC + 64;                // float [2][128]
-  static constexpr int OFF_UNITS = OFF_XCH + 2 * kBlockM * 4;  // Unit[4]: decoded units, ring
+  static constexpr int OFF_UNITS = OFF_XCH + XCH_BYTES;        // Unit[4]: decoded units, ring
   static constexpr int OFF_XMAX = OFF_UNITS + 4 * UNIT_BYTES;   // float [2 parities][2 slots][2 halves][128]
-  static constexpr int OFF_XL = OFF_XMAX + 8 * kBlockM * 4;       // float [2 slots][2 halves][128]
-  static constexpr int END = OFF_XL + 4 * kBlockM * 4;
+  static constexpr int OFF_XL = OFF_XMAX + 8 * kBlockM * 4;     // float [2 slots][2 halves][128]
+  static constexpr int END = OFF_XMAX + XM_BYTES;
   // +1 KB to align the dynamic base to 1024; at least ~117 KB so that only
   // one block (which owns all 512 TMEM columns) is resident per SM.
   static constexpr int SMEM_BYTES = (END + 1024) > 120 * 1024 ? (END + 1024) : 120 * 1024;
@@ -596,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_pb = pb_tag[st] != tag;
           }
           const uint32_t tx = kStageTx + (load_pb ? static_cast<uint32_t>(L::PB_BYTES) : 0u) +
-                              ((kEvo && p.has_mb) ? static_cast<uint32_t>(L::MB_BYTES) : 0u);
+                              ((L::MB_BYTES > 0 && p.has_mb) ? static_cast<uint32_t>(L::MB_BYTES) : 0u);
           ptx::mbar_arrive_expect_tx(&kv_full[st], tx);
           if (!skip) {
 #pragma unroll
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                t * kBlockN + 32 * bx, U.row0[0], U.pb_h, U.pb_b, pol_reuse);
             pb_tag[st] = tag;
           }
-          if (kEvo && p.has_mb) {
+          if (L::MB_BYTES > 0 && p.has_mb) {
 #pragma unroll
             for (int s = 0; s < 2; ++s)
               ptx::tma_load_2d(smem + L::OFF_MB + st * L::MB_BYTES + s * kBlockN * 4, &tmMB, &kv_full[st],
@@ -937,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
         float gsig[kEvo ? OUT_H : 1];
         if (kEvo) {
-          // out = sigmoid(gate) * O / l, sigmoid(g) = 1 / (1 + 2^(-g log2 e))
+          // out = sigmoid(gate) * O / l, sigmoid(g) = (1 + tanh(g / 2)) / 2 (one MUFU op)
           const bool row_ok = e_i < p.Lq && e_valid;
           const uint4* g4 = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.gate) + orow_off +
                                                            half * OUT_H);
@@ -948,8 +950,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[w]));
-              gsig[8 * q + 2 * w] = ptx::rcp(1.f + ptx::ex2(-gf.x * kLog2e)) * inv;
-              gsig[8 * q + 2 * w + 1] = ptx::rcp(1.f + ptx::ex2(-gf.y * kLog2e)) * inv;
+              gsig[8 * q + 2 * w] = fmaf(0.5f, ptx::tanh_approx(0.5f * gf.x), 0.5f) * inv;
+              gsig[8 * q + 2 * w + 1] = fmaf(0.5f, ptx::tanh_approx(0.5f * gf.y), 0.5f) * inv;
             }
           }
         }

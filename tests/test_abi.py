@@ -155,11 +155,11 @@ def test_decode_rejects(L):
 
 
 def test_decode_split_arithmetic():
-    """Host split rule (mirrors csrc/decode.h): enough CTAs for twice the
-    SMs, every split a whole number of 128-key tiles, no empty split."""
+    """Host split rule (mirrors csrc/decode.h): enough CTAs for sixteen per
+    SM, every split a whole number of 128-key tiles, none past the cache."""
     def split(B, Hkv, Lmax, sms):
         tiles = (Lmax + 127) // 128
-        ns = max(1, min(tiles, -(-2 * sms // (B * Hkv))))
+        ns = max(1, min(tiles, -(-16 * sms // (B * Hkv))))
         per = -(-tiles // ns)
         return -(-tiles // per), per * 128
     for B, Hkv, Lmax in ((16, 8, 8192), (1, 1, 100), (2, 8, 65536), (64, 8, 1024)):
