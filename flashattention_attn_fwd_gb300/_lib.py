@@ -23,6 +23,7 @@ FL_ERR_DEVICE_BOUNDS = 6
 MASKS = {"none": 0, "causal": 1, "window": 2, "prefix_lm": 3, "document": 4}
 SCORE_MODS = {"none": 0, "alibi": 1, "softcap": 2}
 FL_DEBUG_SKIP_KV_LOAD = 0x1
+FL_DEBUG_KEY_SPLIT = 0x2
 
 # Every symbol include/flattn.h declares.
 EXPORTS = (

@@ -12,7 +12,7 @@ import math
 import torch
 
 from . import _lib
-from ._lib import FL_DEBUG_SKIP_KV_LOAD, MASKS, SCORE_MODS, FlattnError  # noqa: F401
+from ._lib import FL_DEBUG_KEY_SPLIT, FL_DEBUG_SKIP_KV_LOAD, MASKS, SCORE_MODS, FlattnError  # noqa: F401
 
 
 def _stream_ptr(stream) -> int:

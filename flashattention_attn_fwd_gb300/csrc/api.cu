@@ -236,6 +236,30 @@ fl_status fill_attn_params(const fl_attn_desc& d, const Strides& so, uint32_t* s
   return FL_OK;
 }
 
+// Key split of a last, partial wave.  Units are dealt to the persistent CTAs
+// in turn, so with U units on W CTAs, R = U mod W of them run alone after
+// the full waves while W - R CTAs idle.  When R <= W / 2 each of those R
+// units becomes two key-split units (one per query tile, each walking its
+// key range in two halves on the two slots): the last wave then takes half
+// as long.  FL_DEBUG_KEY_SPLIT splits every unit.
+void plan_key_split(const fl_attn_desc& d, int sm_count, KParams* p) {
+  p->ks_count = 0;
+  if (!fl::key_split_ok(d.d, d.dv)) return;
+  const int units = p->num_units;
+  if (d.debug_flags & FL_DEBUG_KEY_SPLIT) {
+    if (units > 0x3fffffff) return;
+    p->ks_count = 2 * units;
+    p->num_units = 2 * units;
+    return;
+  }
+  const int w = units < sm_count ? units : sm_count;
+  if (w < 2 || units <= w) return;
+  const int r = units % w;
+  if (r == 0 || 2 * r > w) return;
+  p->ks_count = 2 * r;
+  p->num_units = units + r;
+}
+
 }  // namespace
 
 namespace fl {
@@ -282,6 +306,7 @@ fl_status attn_fwd_launch(const void* q, const void* k, const void* v, void* out
   KParams p{};
   const fl_status fs = fill_attn_params(d, so, status, &p);
   if (fs != FL_OK) return fs;
+  plan_key_split(d, sm_count, &p);
   p.out = out;
   p.lse = lse;
   const int64_t units = p.num_units;
@@ -367,6 +392,9 @@ fl_status fl_attn_schedule(const fl_attn_desc* desc, const int32_t* doc_offsets_
   KParams p{};
   const fl_status fs = fill_attn_params(d, so, nullptr, &p);
   if (fs != FL_OK) return fs;
+  // the last-wave split depends on the SM count and leaves the visited tiles
+  // unchanged; the forced split (FL_DEBUG_KEY_SPLIT) is walked as launched
+  if (d.debug_flags & FL_DEBUG_KEY_SPLIT) plan_key_split(d, 1, &p);
   const bool per_slot = d.dv <= 64;  // one MMA thread per slot: per-slot key ranges
   int64_t own = 0, all = 0;
   for (int u = 0; u < p.num_units; ++u) {
@@ -374,7 +402,9 @@ fl_status fl_attn_schedule(const fl_attn_desc* desc, const int32_t* doc_offsets_
     for (int s = 0; s < 2; ++s) {
       const int64_t n = U.hi[s] - U.lo[s] + 1;
       all += n;
-      if (U.valid[s] && U.row0[s] < p.Lq && !(p.slot_mode == fl::SLOT_HEADS && s == 1 && U.hq[1] == U.hq[0]))
+      // a key-split unit's second slot computes the lower half of the rows' keys
+      if (U.ks || (U.valid[s] && U.row0[s] < p.Lq &&
+                   !(p.slot_mode == fl::SLOT_HEADS && s == 1 && U.hq[1] == U.hq[0])))
         own += n;
     }
   }

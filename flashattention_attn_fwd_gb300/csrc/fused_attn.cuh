@@ -37,10 +37,11 @@
 // The online softmax keeps (m, l) per row in the log2 domain.  The
 // reference max m is only raised when a new tile's max exceeds it by more
 // than 8 (a factor 256), so O is rescaled rarely; O and l always use the
-// same m, so the final O / l is exact whatever m was used.  A fixed share of
-// the exponentials is evaluated on the FMA pipe (Cody-Waite split plus a
-// fitted cubic) instead of the MUFU unit, which alone would take longer per
-// tile than the tensor core.
+// same m, so the final O / l is exact whatever m was used.  Optionally
+// (FL_EMU_*) a share of the exponentials is evaluated on the FMA pipe
+// (Cody-Waite split plus a fitted cubic) instead of the MUFU unit; on sm_103a
+// the MUFU unit keeps up with the tensor core at d = 64, so the share is 0 by
+// default.
 //
 // Every mbarrier wait is bounded (KParams::timeout_ns).  When one runs out
 // the block records FL_ERR_TIMEOUT in the status word, every role leaves
@@ -112,13 +113,16 @@ struct EmuPairs {
   static_assert(value >= 0 && value <= 16, "share of FMA-pipe exponentials");
 };
 
-// In units where both slots walk the same key tiles, the two slots'
-// exponent phases (the MUFU-bound part of the softmax) take turns: a slot
-// waits for the other slot's previous phase to end, so that each slot's
-// loads, maxima and waits overlap the other slot's exponentials.  It only
-// orders work: the wait gives up quietly after kTurnWaitNs.
+// Optionally (FL_PINGPONG=1), in units where both slots walk the same key
+// tiles, the two slots' exponent phases take turns: a slot waits for the
+// other slot's previous phase to end, so that each slot's loads, maxima and
+// waits overlap the other slot's exponentials.  It only orders work: the
+// wait gives up quietly after kTurnWaitNs.  The MUFU unit of sm_103a
+// sustains about 32 ex2 per clock per SM, enough for both slots at once, and
+// the turns cost more than they save on the score-modified variants: off by
+// default.
 #ifndef FL_PINGPONG
-#define FL_PINGPONG 1
+#define FL_PINGPONG 0
 #endif
 constexpr uint64_t kTurnWaitNs = 1500;
 
@@ -168,8 +172,8 @@ struct Layout {
   static constexpr int OFF_BAR = OFF_MB + STAGES * MB_BYTES;
   // barriers: q_full[4] q_empty[4] kv_full[S] kv_empty[S] s_full[2] s_free[2]
   //           p_full[2] pv_done[2] o_empty[2] drain[2] xch_full[1] stagger[1]
-  //           o_staged[2] xm_bar[8] xl_bar[8] exp_turn[2]
-  static constexpr int NBARS = 42 + 2 * STAGES;
+  //           o_staged[2] xm_bar[8] xl_bar[8] exp_turn[2] ks_full[1]
+  static constexpr int NBARS = 43 + 2 * STAGES;
   static_assert(NBARS <= 64, "barrier area");
   static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int OFF_XCH = OFF_MISC + 64;                // float [2][128]
@@ -195,6 +199,9 @@ struct Unit {
   int lo[2], hi[2];  // key tiles each slot walks (inclusive, walked from hi down)
   int kv_lo, kv_hi;  // union of the slots' ranges: the tiles the load warp fetches
   int pb_b, pb_h;    // Evoformer: pair-bias tile coordinates
+  int ks;            // key-split unit: both slots hold the same query rows,
+                     // slot 0 the upper and slot 1 the lower half of the key
+                     // range; their tiles alternate in the ring
 };
 static_assert(sizeof(Unit) <= 128, "unit ring entry");
 
@@ -248,9 +255,19 @@ __device__ __forceinline__ Sched make_sched(const KParams& p) {
   return s;
 }
 
+// Ring position of slot s's first own tile within a unit, and the distance
+// between its consecutive own tiles.
+__host__ __device__ __forceinline__ int ring_first(const Unit& U, int s) { return U.ks ? s : U.kv_hi - U.hi[s]; }
+__host__ __device__ __forceinline__ int ring_stride(const Unit& U) { return U.ks ? 2 : 1; }
+// Key tile the load warp fetches at ring position i of a unit.
+__host__ __device__ __forceinline__ int ring_tile(const Unit& U, int i) {
+  return U.ks ? U.hi[i & 1] - (i >> 1) : U.kv_hi - i;
+}
+
 template <int KIND>
-__host__ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, bool per_slot) {
+__host__ __device__ __forceinline__ Unit decode_base(const KParams& p, int u, bool per_slot) {
   Unit U;
+  U.ks = 0;
   U.pb_b = 0;
   U.pb_h = 0;
   U.mbrow[0] = U.mbrow[1] = 0;
@@ -376,6 +393,47 @@ __host__ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, bo
   return U;
 }
 
+// Work unit u.  A key-split unit (the last ks_count units) takes one query
+// tile of a base unit and hands each slot half of that tile's key range:
+// slot 0 the upper ceil(n/2) tiles, slot 1 the lower floor(n/2); the
+// epilogue merges the two partial (m, l, O) of every row.  A tile with a
+// single key tile (or a padding tile) is not split: it runs as a unit whose
+// second slot is a dropped copy of the first.
+template <int KIND>
+__host__ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u, bool per_slot) {
+  const int ks_first = p.num_units - p.ks_count;
+  if (KIND != KIND_ATTN || !per_slot || u < ks_first) return decode_base<KIND>(p, u, per_slot);
+  const int j = u - ks_first;
+  Unit U = decode_base<KIND>(p, ks_first + (j >> 1), per_slot);
+  const bool s1 = (j & 1) != 0;
+  // selects rather than a runtime index: U stays in registers
+  const bool real = (s1 ? U.valid[1] : U.valid[0]) && (s1 ? U.row0[1] : U.row0[0]) < p.Lq &&
+                    !(p.slot_mode == SLOT_HEADS && s1 && U.hq[1] == U.hq[0]);
+  const int lo = s1 ? U.lo[1] : U.lo[0], hi = s1 ? U.hi[1] : U.hi[0];
+  U.b[0] = U.b[1] = s1 ? U.b[1] : U.b[0];
+  U.hq[0] = U.hq[1] = s1 ? U.hq[1] : U.hq[0];
+  U.hkv[0] = U.hkv[1] = s1 ? U.hkv[1] : U.hkv[0];
+  U.row0[0] = U.row0[1] = s1 ? U.row0[1] : U.row0[0];
+  U.valid[0] = real;
+  U.valid[1] = 0;
+  U.kv_lo = lo;
+  U.kv_hi = hi;
+  const int n = hi - lo + 1;
+  if (real && n >= 2) {
+    const int n0 = (n + 1) >> 1;
+    U.ks = 1;
+    U.lo[0] = hi - n0 + 1;
+    U.hi[0] = hi;
+    U.lo[1] = lo;
+    U.hi[1] = lo + (n - n0) - 1;
+  } else {
+    U.ks = 0;
+    U.lo[0] = U.lo[1] = lo;
+    U.hi[0] = U.hi[1] = hi;
+  }
+  return U;
+}
+
 // ------------------------------------------------------------ bounded waits
 struct Ctl {
   volatile uint32_t* abort;
@@ -488,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xm_bar = bars + 24 + 2 * S;    // [slot * 4 + quad]: half-row maxima exchanged
   uint64_t* xl_bar = bars + 32 + 2 * S;    // [slot * 4 + quad]: half-row sums exchanged
   uint64_t* exp_turn = bars + 40 + 2 * S;  // [slot]: the other slot's exponent phase is over
+  uint64_t* ks_full = bars + 42 + 2 * S;   // key-split unit: slot 1's (m, l) published
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   float* xch = reinterpret_cast<float*>(smem + L::OFF_XCH);
   // The TMA thread decodes each unit once and publishes it here before
@@ -529,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(&exp_turn[0], kSoftmaxWarps / 2);
     ptx::mbar_init(&exp_turn[1], kSoftmaxWarps / 2);
+    ptx::mbar_init(ks_full, kSoftmaxWarps / 2);
     misc[1] = 0u;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -584,13 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_iss[qi] = static_cast<int>(qph);
         }
         if (!ok) break;
-        for (int t = U.kv_hi; t >= U.kv_lo; --t, ++it) {
+        const int n_ring = U.kv_hi - U.kv_lo + 1;
+        for (int i = 0; i < n_ring; ++i, ++it) {
+          const int t = ring_tile(U, i);
           const int st = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
           FL_TR(5, it, 0);
           if (!wait_bar(&kv_empty[st], ph ^ 1u, ctl, 2)) { ok = false; break; }
           FL_TR(5, it, 1);
-          const bool skip = p.dbg_skip_tile >= 0 && blockIdx.x == 0 && uc == 0 && (U.kv_hi - t) == p.dbg_skip_tile;
+          const bool skip = p.dbg_skip_tile >= 0 && blockIdx.x == 0 && uc == 0 && i == p.dbg_skip_tile;
           int tag = -1;
           bool load_pb = false;
           if (KIND == KIND_EVO && p.has_pb) {
@@ -634,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // release the stage on behalf of a slot that does not use this tile
 #pragma unroll
           for (int s = 0; s < 2; ++s)
-            if (t < U.lo[s] || t > U.hi[s]) ptx::mbar_arrive(&kv_empty[st]);
+            if (U.ks ? s != (i & 1) : (t < U.lo[s] || t > U.hi[s])) ptx::mbar_arrive(&kv_empty[st]);
           kv_count = it + 1;
         }
         if (!ok) break;
@@ -707,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int u = sch.first;
       auto first_idx = [&](const Unit& V, uint32_t base) -> uint32_t {
-        return base + static_cast<uint32_t>(V.kv_hi - V.hi[s]);
+        return base + static_cast<uint32_t>(ring_first(V, s));
       };
       auto first_s = [&](uint32_t ucn, uint32_t idx) -> bool {
         if (!wait_bar(&kv_full[idx % S], (idx / S) & 1u, ctl, 11)) return false;
@@ -724,13 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_issued = false;
         const uint32_t qb = uc % L::QBUF;
         const int un = u + sch.step;
+        const uint32_t stride = static_cast<uint32_t>(ring_stride(Us));
         for (int k = 0; k < ns && ok; ++k) {
-          const uint32_t idx = idx0 + k;
+          const uint32_t idx = idx0 + k * stride;
+          const uint32_t idn = idx + stride;
           const int st = static_cast<int>(idx % S);
           FL_TR(s, idx, 0);
           if (k + 1 < ns) {
-            if (!wait_bar(&kv_full[(idx + 1) % S], ((idx + 1) / S) & 1u, ctl, 15)) { ok = false; break; }
-            if (!issue_s(s, qb, static_cast<int>((idx + 1) % S))) { ok = false; break; }
+            if (!wait_bar(&kv_full[idn % S], (idn / S) & 1u, ctl, 15)) { ok = false; break; }
+            if (!issue_s(s, qb, static_cast<int>(idn % S))) { ok = false; break; }
           } else if (kCross && un < sch.end) {
             // next unit's first own tile, if its ring index is less than S
             // ahead of this (still unreleased) one
@@ -845,6 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float xmul = kRaw ? scale_log2 : (kEvo ? kLog2e : 1.0f);
     constexpr int kEmu = EmuPairs<KIND, SCORE>::value;
     uint32_t scnt = 0, uc = 0, it = 0;
+    uint32_t kscnt = 0;  // slot 0: key-split merges done so far
     uint32_t pc = 0;  // P tiles handed to the MMA warp so far (= P V launched for this slot)
     constexpr bool kPingPong = kPerSlot && FL_PINGPONG;
     uint32_t tcnt = 0;  // exponent phases taken in turns so far
@@ -866,6 +931,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA when it fits (DV <= D, or half the channels for differential
     // attention), else written by each thread straight to global memory.
     constexpr bool kTmaOut = OUT_COLS * 2 * kBlockM <= L::Q_BYTES;
+    // key-split units (attention only; the host enables them only where
+    // key_split_ok holds)
+    constexpr bool kKs = KIND == KIND_ATTN && key_split_ok(D, DV);
+    static_assert(!kKs || (kPerSlot && kTmaOut && kRowSplit == 1 && S >= 3),
+                  "key split needs per-slot MMA, staged output and three ring stages");
     const bool leader = lane == 0 && sw == 4 * kRowSplit * s;
     int pending_qi = -1;  // leader: Q buffer whose bulk store may still be reading it
     bool have_prev = false;
@@ -1037,6 +1107,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, !*ctl.abort);
     };
 
+    // Epilogue of a key-split unit, run right after the unit's last tile
+    // (never deferred; only tail units are split).  Slot 1 hands its row
+    // (m, l) to slot 0 through its own Q buffer (idle: its last S is done)
+    // and leaves O1 in TMEM; slot 0 rescales both halves to the larger
+    // reference max, merges them, stores the tile, and releases slot 1's O
+    // columns and Q buffer.
+    auto epilogue_ks = [&](const Epi& e) -> bool {
+      const Unit& Ue = unit_at(e.uc);
+      if (!__all_sync(0xffffffffu, wait_bar(&pv_done[s], e.pcl & 1u, ctl, 30 + s))) return false;
+      ptx::tc_fence_after();
+      const int qi = static_cast<int>(e.uc % L::QBUF) * 2;  // slot 0's Q buffer; slot 1's is qi + 1
+      float* xq = reinterpret_cast<float*>(smem + L::OFF_Q + (qi + 1) * L::Q_BYTES);
+      if (s == 1) {
+        xq[r] = e.m;
+        xq[kBlockM + r] = e.l;
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&o_staged[1]);  // one phase per unit, as in the other units
+          ptx::mbar_arrive(ks_full);
+        }
+        return __all_sync(0xffffffffu, !*ctl.abort);
+      }
+      if (!__all_sync(0xffffffffu, wait_bar(ks_full, kscnt & 1u, ctl, 38))) return false;
+      ++kscnt;
+      ptx::tc_fence_after();
+      const float m1 = xq[r], l1 = xq[kBlockM + r];
+      const float mrow = fmaxf(e.m, m1);
+      const float w0 = e.m == -CUDART_INF_F ? 0.f : ptx::ex2(e.m - mrow);
+      const float w1 = m1 == -CUDART_INF_F ? 0.f : ptx::ex2(m1 - mrow);
+      const float lrow = e.l * w0 + l1 * w1;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      const float k0 = w0 * inv, k1 = w1 * inv;
+      // O = (O0 w0 + O1 w1) / l, O1 in the columns after O0
+      uint32_t packed[DV / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t a[32], b1[32];
+        ptx::tmem_ld32(tO + c0, a);
+        ptx::tmem_ld32(tO + DV + c0, b1);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(a);
+        ptx::reg_fence32(b1);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          packed[c0 / 2 + q] =
+              ptx::pack_bf16x2(fmaf(__uint_as_float(b1[2 * q]), k1, __uint_as_float(a[2 * q]) * k0),
+                               fmaf(__uint_as_float(b1[2 * q + 1]), k1, __uint_as_float(a[2 * q + 1]) * k0));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&o_empty[0]);
+        ptx::mbar_arrive(&o_empty[1]);
+      }
+      const int e_i = Ue.row0[0] + r;
+      if (e_i < p.Lq && p.lse && Ue.valid[0])
+        p.lse[(static_cast<int64_t>(Ue.b[0]) * p.Hq + Ue.hq[0]) * p.Lq + e_i] =
+            (lrow > 0.f ? mrow + __log2f(lrow) : -CUDART_INF_F) * kLn2;
+      // the tile through slot 0's staging buffer, as in the epilogue above
+      constexpr int ROWB = L::ROWB_V;
+      constexpr int BOXC = ROWB / 2;
+      constexpr uint32_t SWM = ROWB == 128 ? 7u : (ROWB == 64 ? 3u : 1u);
+      uint8_t* stage = smem + L::OFF_Q + qi * L::Q_BYTES;
+#pragma unroll
+      for (int q = 0; q < DV / 8; ++q) {
+        const int col = 8 * q;
+        uint32_t off = static_cast<uint32_t>(r * ROWB + (col % BOXC) * 2);
+        off ^= ((off >> 7) & SWM) << 4;
+        *reinterpret_cast<uint4*>(stage + (col / BOXC) * kBlockM * ROWB + off) =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&o_staged[0]);
+      if (leader && wait_bar(&o_staged[0], e.uc & 1u, ctl, 34)) {
+        if (Ue.valid[0]) {
+#pragma unroll
+          for (int bx = 0; bx < DV / BOXC; ++bx)
+            ptx::tma_store_4d(&tmO, stage + bx * kBlockM * ROWB, bx * BOXC, Ue.row0[0], Ue.hq[0], Ue.b[0]);
+          ptx::bulk_commit_group();
+        }
+        pending_qi = qi;
+        // every warp of slot 0 has read (m, l) from slot 1's Q buffer
+        ptx::mbar_arrive(&q_empty[qi + 1]);
+        if (!kDefer) release_pending();
+      }
+      return __all_sync(0xffffffffu, !*ctl.abort);
+    };
+
     for (int u = sch.first; u < sch.end && ok; u += sch.step, ++uc) {
       if (lane == 0 && sw == 0) FL_TR(4, 32 + uc, 0);
       // the previous unit's output store must have read its staging buffer
@@ -1052,7 +1212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ns = u_hi - Us.lo[s] + 1;
       const bool turns = kPingPong && Us.lo[0] == Us.lo[1] && Us.hi[0] == Us.hi[1];
       const int n = Us.kv_hi - Us.kv_lo + 1;
-      const uint32_t idx0 = it + static_cast<uint32_t>(Us.kv_hi - u_hi);
+      // ring index of this slot's first tile (only the Evoformer kinds read
+      // the ring from here; their units are never key-split: stride 1)
+      const uint32_t idx0 = it + static_cast<uint32_t>(ring_first(Us, s));
       const int i = u_row0 + r;
       const int ic = i < p.Lq ? i : p.Lq - 1;
       int lo, hi;
@@ -1089,6 +1251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* pb_st = smem + L::OFF_PB + (idx % S) * L::PB_BYTES;
         const float* mb_st = reinterpret_cast<const float*>(smem + L::OFF_MB + (idx % S) * L::MB_BYTES) + s * kBlockN;
         float cmax[NBLK];
+        // one vote per tile decides whether any block needs the mask
+        const bool tile_part = __any_sync(0xffffffffu, (j0 < lo) || (j0 + kHalfCols - 1 > hi));
         // Score transform and max, 32 columns at a time: the first block
         // while the others are still being read from TMEM.
 #pragma unroll
@@ -1182,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // mask (only when some row of this warp sees part of this block)
-          if (__any_sync(0xffffffffu, (j0 + c0 < lo) || (j0 + c0 + 31 > hi))) {
+          if (tile_part && __any_sync(0xffffffffu, (j0 + c0 < lo) || (j0 + c0 + 31 > hi))) {
             const int clo = lo - j0, chi = hi - j0;
 #pragma unroll
             for (int c = c0; c < c0 + 32; ++c)
@@ -1318,7 +1482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && sw == 0) FL_TR(4, 32 + uc, 3);
       {
         const Epi cur{uc, pc - 1, m, l};
-        if (kDefer) {
+        if (kKs && Us.ks) {
+          if (!epilogue_ks(cur)) {
+            ok = false;
+            break;
+          }
+        } else if (kDefer) {
           prev = cur;
           have_prev = true;
         } else if (!epilogue(cur)) {

@@ -46,6 +46,16 @@ constexpr int kCtlRegs = kRowSplit == 1 ? 56 : 32;
 constexpr int kSoftmaxRegs = kRowSplit == 1 ? 224 : 112;
 static_assert(128 * kCtlRegs + 32 * kSoftmaxWarps * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 
+// Key-split units (two slots on the same query rows, halves of the key
+// range) need one MMA thread per slot (DV <= 64), the output tile staged in
+// a Q buffer (DV <= D), one softmax thread per row, and a ring of at least
+// three stages (a slot's next own tile is two ring positions ahead of the
+// one it still holds), which D <= 64 leaves room for.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr bool key_split_ok(int d, int dv) { return dv <= d && d <= 64 && kRowSplit == 1; }
+
 struct KParams {
   // problem (Evoformer row-wise: B is B * N_seq, Hq == Hkv == H;
   // column-wise: Hq == Hkv == H * N_res, rows are MSA rows)
@@ -56,6 +66,11 @@ struct KParams {
   int pairs_per_group;  // SLOT_HEADS: ceil(group / 2)
   int num_units;
   int chunked;          // 1: each CTA takes a contiguous range of units
+  // The last ks_count units are key-split units (attention, DV <= 64): unit
+  // num_units - ks_count + j takes query tile (j & 1) of base unit
+  // num_units - ks_count + (j >> 1) and walks its key range in two halves,
+  // one per slot, merged in the epilogue.  0: none.
+  int ks_count;
   float scale_log2;     // scale * log2(e)
   float scale;          // scale (natural units; Evoformer)
 

@@ -78,6 +78,12 @@ typedef enum {
                                       of its first work unit: its pipeline
                                       wait runs out and the call reports
                                       FL_ERR_TIMEOUT (tests the bounded waits) */
+#define FL_DEBUG_KEY_SPLIT 0x2u    /* fl_attn_fwd with dv <= d <= 64: every
+                                      work unit is split along the key axis
+                                      (normally only the units of a last,
+                                      partial wave over the SMs are), so that
+                                      small problems exercise the split and
+                                      its merge */
 
 /*
  * Problem descriptor for fl_attn_fwd / fl_diffattn_fwd.
@@ -133,6 +139,8 @@ FL_API fl_status fl_attn_fwd(const void* q, const void* k, const void* v, void* 
  *   tiles[0]  (query tile, key tile) pairs computed for rows that exist,
  *   tiles[1]  the same including the padding slot of an odd tile count,
  *   tiles[2]  the dense count B * Hq * ceil(Lq/128) * ceil(Lk/128).
+ * With FL_DEBUG_KEY_SPLIT in desc->debug_flags the walk is that of the
+ * forced key split (tiles[0] is unchanged by the split).
  * doc_offsets_host: host copy of the document offsets (DOCUMENT only).
  * Pointers in desc other than doc offsets are not read.
  */

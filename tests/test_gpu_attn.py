@@ -13,7 +13,7 @@ import torch
 import oracle
 from flashattention_attn_fwd_gb300 import (FlattnError, attn_fwd, diffattn_fwd, evoformer_col_gated_attn_fwd,
                                            evoformer_gated_attn_fwd, synth, sync_status)
-from flashattention_attn_fwd_gb300._lib import FL_DEBUG_SKIP_KV_LOAD, FL_ERR_TIMEOUT
+from flashattention_attn_fwd_gb300._lib import FL_DEBUG_KEY_SPLIT, FL_DEBUG_SKIP_KV_LOAD, FL_ERR_TIMEOUT
 
 pytestmark = pytest.mark.gpu
 
@@ -170,6 +170,51 @@ def test_attn_many_units_per_cta_sampled_rows(case):
     gl = np.array([lc[b, h, i].item() for b, h, i in rows])
     assert np.abs(g - ro).max() <= ATOL and np.linalg.norm(g - ro) / np.linalg.norm(ro) <= RTOL
     assert np.abs(gl - rl).max() <= LSE_ATOL
+
+
+KEY_SPLIT = [
+    # (B, Hq, Hkv, L, d, dv, n_docs, kwargs), run with every unit split along
+    # the key axis: the two halves of each query tile's key range are merged
+    # through their (m, l) -- odd and even tile counts, single-tile ranges
+    # (not split), padding tiles, every mask, both score mods, GQA
+    (1, 2, 2, 256, 64, 64, None, dict()),
+    (1, 2, 2, 640, 64, 64, None, dict()),
+    (2, 3, 3, 300, 64, 64, None, dict(mask="causal")),
+    (1, 2, 2, 1000, 64, 64, None, dict(mask="window", window=300)),
+    (1, 2, 2, 700, 64, 64, None, dict(mask="prefix_lm", prefix=200)),
+    (2, 4, 4, 900, 64, 64, 4, dict(mask="document")),
+    (1, 8, 2, 600, 64, 64, None, dict(mask="causal")),
+    (1, 6, 2, 520, 64, 64, None, dict()),
+    (1, 2, 2, 500, 64, 64, None, dict(score_mod="alibi")),
+    (1, 2, 2, 500, 64, 64, None, dict(score_mod="softcap", softcap=20.0)),
+    (1, 2, 2, 400, 32, 32, None, dict(mask="causal")),
+    (1, 2, 2, 400, 128, 64, None, dict(mask="causal")),
+    (1, 2, 2, 300, 64, 32, None, dict()),
+]
+
+
+@pytest.mark.parametrize("case", KEY_SPLIT, ids=lambda c: f"B{c[0]}H{c[1]}x{c[2]}L{c[3]}d{c[4]}dv{c[5]}-" +
+                         "-".join(f"{k}{v}" for k, v in c[7].items()))
+def test_attn_forced_key_split(case):
+    B, Hq, Hkv, L, d, dv, nd, kw = case
+    (q, k, v, offs, slopes), out, lse = run_attn(B, Hq, Hkv, L, d, seed=3 * L + d, n_docs=nd, dv=dv,
+                                                 debug_flags=FL_DEBUG_KEY_SPLIT, **kw)
+    ro, rl = oracle.attention(q, k, v, **_oracle_kw(kw, offs, slopes))
+    check(out, ro, lse, rl)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(score_mod="softcap", softcap=30.0), dict(mask="window", window=200)],
+                         ids=["none", "softcap", "window"])
+def test_attn_last_wave_key_split(kw):
+    """More units than SMs with a short last wave (at most half the SMs): the
+    last wave's units run key-split; the whole output against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # L = 512: two units (query-tile pairs) per head; units = B * H * 2
+    H = (sms + 8) // 2
+    (q, k, v, offs, slopes), out, lse = run_attn(1, H, H, 512, 64, seed=sms, **kw)
+    assert (2 * H) % sms != 0 and 2 * ((2 * H) % sms) <= sms
+    ro, rl = oracle.attention(q, k, v, **_oracle_kw(kw, offs, slopes))
+    check(out, ro, lse, rl)
 
 
 def test_causal_row0_is_v0_bit_exact():

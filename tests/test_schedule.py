@@ -76,3 +76,18 @@ def test_schedule_value_dim_128_walks_the_union():
     slots, which then walk the union of their ranges: never fewer blocks."""
     own, _, _ = _schedule(1, 4, 4, 2048, 64, 128, mask_kind=1)
     assert own >= 4 * _visible_blocks("causal", 2048)
+
+
+@pytest.mark.parametrize("L", [256, 300, 2100])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[3]}")
+@pytest.mark.parametrize("heads", [(4, 4), (6, 2)], ids=["mha", "gqa3"])
+def test_key_split_schedule_visits_the_same_blocks(L, case, heads):
+    """Splitting every unit along the key axis (two slots on the same query
+    rows, halves of the key range) visits exactly the visible blocks too:
+    the halves neither overlap nor leave a gap."""
+    mask, _, dkw, okw = case
+    Hq, Hkv = heads
+    B = 2
+    own, allt, _ = _schedule(B, Hq, Hkv, L, 64, 64, debug_flags=_lib.FL_DEBUG_KEY_SPLIT, **dkw)
+    assert own == B * Hq * _visible_blocks(mask, L, **okw)
+    assert allt >= own
