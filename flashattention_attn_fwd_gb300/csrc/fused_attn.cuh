@@ -922,9 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t uc, pcl;  // unit counter; index of the unit's last P V completion
       float m, l;
     };
-    // With two Q buffers the epilogue of a unit runs after the next unit's
-    // first tile (its last P V has finished by then, and that tile's softmax
-    // overlaps the wait), and the bulk store's hold on the staging buffer is
+    // With two Q buffers the epilogue of a unit runs when the next unit
+    // starts (its last P V completes meanwhile, and the next unit's first S
+    // is already issued), and the bulk store's hold on the staging buffer is
     // released at the next tile instead of being waited for.
     constexpr bool kDefer = L::QBUF == 2;
     // Output tile of one slot: staged in the slot's Q buffer and stored by
@@ -1226,6 +1226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      // the previous unit's epilogue: outside the tile loop, which stays small
+      // (its last P V is done or nearly so; this unit's first S is already
+      // in flight)
+      if (kDefer && have_prev) {
+        have_prev = false;
+        if (!epilogue(prev)) {
+          ok = false;
+          break;
+        }
+      }
       for (int k = 0; k < ns; ++k, ++scnt) {
         const int t = u_hi - k;
         const int j0 = t * kBlockN + c_off;   // key of this thread's first column
@@ -1472,10 +1482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&p_full[s]);
         if (tr) FL_TR(2 + s, scnt, 6);
         ++pc;
-        if (kDefer && k == 0 && have_prev) {
-          have_prev = false;
-          if (!epilogue(prev)) { ok = false; break; }
-        }
       }
       if (!ok) break;
       it += n;
