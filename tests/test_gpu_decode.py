@@ -40,6 +40,8 @@ CASES = [
     (2, 8, 2, 1, 640, 64, dict(score_mod="softcap", softcap=5.0)),
     (4, 4, 1, 16, 256, 64, dict(causal=True)),
     (1, 64, 1, 1, 129, 64, dict()),
+    (2, 8, 2, 1, 100, 64, dict(causal=True)),
+    (2, 16, 2, 1, 1500, 128, dict(score_mod="alibi")),
 ]
 
 
