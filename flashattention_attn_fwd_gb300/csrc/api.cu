@@ -448,7 +448,7 @@ fl_status decode_check(const void* q, const void* k, const void* v, void* out, f
 }
 
 size_t decode_workspace(const fl_attn_desc& d, int sm_count, int* n_split, int* chunk) {
-  fl::decode_split(d.B, d.Hkv, d.Lk, sm_count, n_split, chunk);
+  fl::decode_split(d.B, d.Hkv, d.Lk, d.Hq / d.Hkv * d.Lq, sm_count, n_split, chunk);
   if (*n_split <= 1) return 0;
   const size_t rows = static_cast<size_t>(d.B) * d.Hq * d.Lq;
   return static_cast<size_t>(*n_split) * rows * (static_cast<size_t>(d.d) + 1) * sizeof(float);

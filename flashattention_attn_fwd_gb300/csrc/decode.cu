@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kDecThreads, MR <= 16 ? 2 : 1)
 constexpr int kDwWarps = 8;
 constexpr int kDwThreads = 32 * kDwWarps;
 constexpr int kDwKeys = kDecTileN / kDwWarps;  // keys per warp per tile (16)
-constexpr int kDwRows = 8;                     // query rows per CTA (rows 8..15 of the MMA tile stay empty)
+constexpr int kDwRows = kDecodeWarpRows;       // query rows per CTA (rows 8..15 of the MMA tile stay empty)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"

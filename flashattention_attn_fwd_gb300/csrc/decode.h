@@ -29,13 +29,21 @@ struct DecodeParams {
   int score_mod, causal;
 };
 
-// Number of key splits and keys per split for a problem on `sm_count` SMs:
-// enough CTAs for many waves (cache lengths differ per sequence, and a split
-// past a sequence's length has no work), whole 128-key tiles per split.
-inline void decode_split(int B, int Hkv, int Lmax, int sm_count, int* n_split, int* chunk) {
+// Query rows one CTA of the warp-level decode kernel serves (larger M uses
+// the block-phase kernel).
+constexpr int kDecodeWarpRows = 8;
+
+// Number of key splits and keys per split for a problem on `sm_count` SMs
+// with M = (Hq / Hkv) * Lq query rows per CTA: enough CTAs for several waves
+// (cache lengths differ per sequence, and a split past a sequence's length
+// has no work) -- four per SM for the warp-level kernel, whose CTAs stream
+// longer ranges well, sixteen for the block-phase kernel -- and whole
+// 128-key tiles per split.
+inline void decode_split(int B, int Hkv, int Lmax, int M, int sm_count, int* n_split, int* chunk) {
   const int tiles = (Lmax + 127) / 128;
   const int heads = B * Hkv;
-  int ns = (16 * sm_count + heads - 1) / heads;
+  const int per_sm = M <= kDecodeWarpRows ? 4 : 16;
+  int ns = (per_sm * sm_count + heads - 1) / heads;
   ns = ns < 1 ? 1 : (ns > tiles ? tiles : ns);
   const int tiles_per = (tiles + ns - 1) / ns;
   *chunk = tiles_per * 128;

@@ -155,17 +155,22 @@ def test_decode_rejects(L):
 
 
 def test_decode_split_arithmetic():
-    """Host split rule (mirrors csrc/decode.h): enough CTAs for sixteen per
-    SM, every split a whole number of 128-key tiles, none past the cache."""
-    def split(B, Hkv, Lmax, sms):
+    """Host split rule (mirrors csrc/decode.h): enough CTAs for four per SM
+    (up to 8 query rows per CTA) or sixteen per SM (more rows), every split a
+    whole number of 128-key tiles, none past the cache."""
+    def split(B, Hkv, Lmax, M, sms):
         tiles = (Lmax + 127) // 128
-        ns = max(1, min(tiles, -(-16 * sms // (B * Hkv))))
+        per_sm = 4 if M <= 8 else 16
+        ns = max(1, min(tiles, -(-per_sm * sms // (B * Hkv))))
         per = -(-tiles // ns)
         return -(-tiles // per), per * 128
     for B, Hkv, Lmax in ((16, 8, 8192), (1, 1, 100), (2, 8, 65536), (64, 8, 1024)):
-        ns, chunk = split(B, Hkv, Lmax, 152)
-        assert chunk % 128 == 0 and (ns - 1) * chunk < Lmax <= ns * chunk
-    assert split(1, 1, 100, 152) == (1, 128)
+        for M in (1, 4, 8, 16, 64):
+            ns, chunk = split(B, Hkv, Lmax, M, 152)
+            assert chunk % 128 == 0 and (ns - 1) * chunk < Lmax <= ns * chunk
+    assert split(1, 1, 100, 4, 152) == (1, 128)
+    assert split(16, 8, 8192, 4, 152) == (5, 1664)
+    assert split(16, 8, 8192, 16, 152) == (16, 512)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

@@ -87,3 +87,23 @@ def test_decode_serving_batch_whole_tensor():
     sync_status()
     ro, rl = oracle.decode_attention(q, k, v, kv_len)
     _check(out, lse, ro, rl)
+
+
+def test_decode_workspace_matches_the_split_rule():
+    """fl_attn_decode_workspace_size against the split rule on this GPU's SM
+    count: four CTAs per SM with up to 8 query rows per CTA, sixteen with
+    more; fp32 partial output and log-sum-exp per split and row."""
+    import ctypes
+    from flashattention_attn_fwd_gb300 import _lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, Hq, Hkv, Lq, Lmax, d in ((16, 32, 8, 1, 8192, 64), (4, 32, 2, 1, 4096, 128), (2, 8, 2, 8, 2048, 64),
+                                    (1, 4, 4, 1, 100, 64)):
+        M = Hq // Hkv * Lq
+        tiles = (Lmax + 127) // 128
+        ns = max(1, min(tiles, -(-(4 if M <= 8 else 16) * sms // (B * Hkv))))
+        per = -(-tiles // ns)
+        ns = -(-tiles // per)
+        want = 0 if ns <= 1 else ns * B * Hq * Lq * (d + 1) * 4
+        desc = _lib.new_desc()
+        desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = B, Hq, Hkv, Lq, Lmax, d, d
+        assert _lib.lib().fl_attn_decode_workspace_size(ctypes.byref(desc)) == want
