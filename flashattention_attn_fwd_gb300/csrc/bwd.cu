@@ -109,9 +109,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // L2[buf][128] then Dv[buf][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA: (batch b, key/value head hkv, key tile jt)
-  const int jt = blockIdx.x % p.n_ktiles;
-  const int bh = blockIdx.x / p.n_ktiles;
+  // this CTA: (batch b, key/value head hkv, key tile jt), key tiles in the
+  // outer order so that the first tiles of every head (the longest walks
+  // under causal and prefix masks) start first and the short ones end the grid
+  const int jt = blockIdx.x / (p.B * p.Hkv);
+  const int bh = blockIdx.x % (p.B * p.Hkv);
   const int hkv = bh % p.Hkv, b = bh / p.Hkv;
   const int j0 = jt * 128;
   const int group = p.Hq / p.Hkv;
