@@ -795,15 +795,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (k + 1 < ns) {
             if (!wait_bar(&kv_full[idn % S], (idn / S) & 1u, ctl, 15)) { ok = false; break; }
             if (!issue_s(s, qb, static_cast<int>(idn % S))) { ok = false; break; }
-          } else if (kCross && un < sch.end) {
-            // next unit's first own tile, if its ring index is less than S
-            // ahead of this (still unreleased) one
-            if (!wait_q(uc + 1, s)) { ok = false; break; }
-            const uint32_t idxn = first_idx(unit_at(uc + 1), it + n);
-            if (idxn - idx < static_cast<uint32_t>(S)) {
-              if (!first_s(uc + 1, idxn)) { ok = false; break; }
-              s_issued = true;
-            }
           }
           FL_TR(s, idx, 2);
           if (k == 0 && !wait_bar(&o_empty[s], (uc & 1u) ^ 1u, ctl, 13)) { ok = false; break; }
@@ -814,6 +805,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(s, st, k > 0);
           ptx::mma_commit(&pv_done[s]);
           ptx::mma_commit(&kv_empty[st]);
+          if (k + 1 == ns && kCross && un < sch.end) {
+            // next unit's first own tile, if its ring index is less than S
+            // ahead of this one (issued after the last P V, which the next
+            // unit's epilogue waits for)
+            if (!wait_q(uc + 1, s)) { ok = false; break; }
+            const uint32_t idxn = first_idx(unit_at(uc + 1), it + n);
+            if (idxn - idx < static_cast<uint32_t>(S)) {
+              if (!first_s(uc + 1, idxn)) { ok = false; break; }
+              s_issued = true;
+            }
+          }
         }
         it += n;
         ++uc;
@@ -1208,7 +1210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // this slot's fields of the unit, read straight from shared memory
       const Unit& Us = unit_at(uc);
-      const int u_hi = Us.hi[s], u_b = Us.b[s], u_hq = Us.hq[s], u_row0 = Us.row0[s], u_valid = Us.valid[s];
+      const int u_hi = Us.hi[s], u_b = Us.b[s], u_hq = Us.hq[s], u_row0 = Us.row0[s];
       const int ns = u_hi - Us.lo[s] + 1;
       const bool turns = kPingPong && Us.lo[0] == Us.lo[1] && Us.hi[0] == Us.hi[1];
       const int n = Us.kv_hi - Us.kv_lo + 1;
