@@ -363,6 +363,13 @@ def _oracle_head(args):
 
 def cpu_model() -> str:
     try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5)
+        for ln in r.stdout.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
                 if ln.lower().startswith(("model name", "cpu part", "hardware")):
@@ -405,7 +412,8 @@ def oracle_sample(n_heads: int, seed: int = 0):
             os.environ.pop(k, None)
         else:
             os.environ[k] = v
-    desc = (f"fp64 oracle, {n_heads} (b,h) heads x 3 headline variants of B{B} H{H} L{L} d{D}, "
+    what = "the whole headline step" if n_heads == B * H else f"{n_heads} of the {B * H} (b,h) heads"
+    desc = (f"fp64 oracle, {what} (3 variants of B{B} H{H} L{L} d{D}), "
             f"{workers} worker processes x 1 BLAS thread")
     return flops / wall / 1e12, wall, workers, desc
 
@@ -437,7 +445,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    n_heads = 2
+    n_heads = B * H  # each step: the whole headline step
     for _ in range(args.warmup):
         oracle_sample(n_heads)
     vals, walls = [], []
@@ -452,7 +460,7 @@ def run_reference(args):
         "ms_per_step": round(1e3 * statistics.median(walls), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"score_mod MHA fwd B={B} H={H} L={L} d={D}: ALiBi, softcap 30, "
-                               "causal window 256", "sample_per_step": f"{n_heads} heads x 3 variants"},
+                               "causal window 256", "sample_per_step": f"{n_heads} (b,h) heads x 3 variants"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
                          "workers": workers, "cpu_model": cpu_model(), "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -602,9 +610,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, wall, workers, desc = oracle_sample(n_heads=8)
+        v, wall, workers, desc = oracle_sample(n_heads=B * H)
         cpu = {"value": round(v, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "workers": workers,
-               "cpu_model": cpu_model(), "kind": "oracle", "sample": desc, "wall_s": round(wall, 2)}
+               "cpu_model": cpu_model(), "kind": "oracle", "sample": desc, "wall_s": round(wall, 2),
+               "cpu_s": round(wall * workers, 1)}
 
     if rank == 0:
         line = {

@@ -1265,12 +1265,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         float cmax[NBLK];
         // one vote per tile decides whether any block needs the mask
         const bool tile_part = __any_sync(0xffffffffu, (j0 < lo) || (j0 + kHalfCols - 1 > hi));
+        // Softcap on a tile no row of the warp masks: the whole row first,
+        // one range vote, then the polynomial on every score without
+        // branches; it increases on its range, so the transformed row max is
+        // the polynomial of the raw max.
+        bool loads_done = false, sc_fast = false;
+        if (SCORE == SCORE_SOFTCAP && !tile_part) {
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int b = 1; b < NBLK; ++b) ptx::reg_fence32f(&x[32 * b]);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&s_free[s]);
+          loads_done = true;
+          float hi4[4], lo4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi4[e] = fmaxf(x[e], x[4 + e]);
+            lo4[e] = fminf(x[e], x[4 + e]);
+          }
+#pragma unroll
+          for (int c = 8; c < kHalfCols; c += 8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hi4[e] = ptx::max3(hi4[e], x[c + e], x[c + 4 + e]);
+              lo4[e] = ptx::min3(lo4[e], x[c + e], x[c + 4 + e]);
+            }
+          const float shi = fmaxf(fmaxf(hi4[0], hi4[1]), fmaxf(hi4[2], hi4[3]));
+          const float slo = fminf(fminf(lo4[0], lo4[1]), fminf(lo4[2], lo4[3]));
+          sc_fast = __all_sync(0xffffffffu, shi <= p.sc_smax && slo >= -p.sc_smax);
+          if (sc_fast) {
+            const float2 sq0 = make_float2(p.sc_q[0], p.sc_q[0]), sq1 = make_float2(p.sc_q[1], p.sc_q[1]);
+            const float2 sq2 = make_float2(p.sc_q[2], p.sc_q[2]), sq3 = make_float2(p.sc_q[3], p.sc_q[3]);
+#pragma unroll
+            for (int c = 0; c < kHalfCols; c += 2) {
+              const float2 sv = make_float2(x[c], x[c + 1]);
+              const float2 z = ptx::mul2(sv, sv);
+              float2 q = ptx::fma2(sq3, z, sq2);
+              q = ptx::fma2(q, z, sq1);
+              q = ptx::fma2(q, z, sq0);
+              const float2 v = ptx::mul2(sv, q);
+              x[c] = v.x;
+              x[c + 1] = v.y;
+            }
+            const float z = shi * shi;
+            const float tm = shi * fmaf(fmaf(fmaf(p.sc_q[3], z, p.sc_q[2]), z, p.sc_q[1]), z, p.sc_q[0]);
+#pragma unroll
+            for (int b = 0; b < NBLK; ++b) cmax[b] = tm;
+          }
+        }
         // Score transform and max, 32 columns at a time: the first block
         // while the others are still being read from TMEM.
 #pragma unroll
-        for (int hf = 0; hf < NBLK; ++hf) {
+        for (int hf = 0; hf < NBLK && !sc_fast; ++hf) {
           const int c0 = hf * 32;
-          if (hf == 1) {
+          if (hf == 1 && !loads_done) {
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int b = 1; b < NBLK; ++b) ptx::reg_fence32f(&x[32 * b]);
