@@ -1269,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one range vote, then the polynomial on every score without
         // branches; it increases on its range, so the transformed row max is
         // the polynomial of the raw max.
-        bool loads_done = false, sc_fast = false;
+        bool loads_done = false, row_done = false;  // row_done: the whole row is transformed
         if (SCORE == SCORE_SOFTCAP && !tile_part) {
           ptx::tmem_ld_wait();
 #pragma unroll
@@ -1293,8 +1293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           const float shi = fmaxf(fmaxf(hi4[0], hi4[1]), fmaxf(hi4[2], hi4[3]));
           const float slo = fminf(fminf(lo4[0], lo4[1]), fminf(lo4[2], lo4[3]));
-          sc_fast = __all_sync(0xffffffffu, shi <= p.sc_smax && slo >= -p.sc_smax);
-          if (sc_fast) {
+          row_done = __all_sync(0xffffffffu, shi <= p.sc_smax && slo >= -p.sc_smax);
+          if (row_done) {
             const float2 sq0 = make_float2(p.sc_q[0], p.sc_q[0]), sq1 = make_float2(p.sc_q[1], p.sc_q[1]);
             const float2 sq2 = make_float2(p.sc_q[2], p.sc_q[2]), sq3 = make_float2(p.sc_q[3], p.sc_q[3]);
 #pragma unroll
@@ -1314,10 +1314,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < NBLK; ++b) cmax[b] = tm;
           }
         }
+        // ALiBi and plain scores on such a tile: the same whole-row form (one
+        // straight-line transform and max tree instead of four blocks)
+        if ((SCORE == SCORE_ALIBI || kRaw) && !tile_part) {
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int b = 1; b < NBLK; ++b) ptx::reg_fence32f(&x[32 * b]);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&s_free[s]);
+          loads_done = true;
+          if (SCORE == SCORE_ALIBI) {
+            const float2 cl = make_float2(scale_log2, scale_log2);
+            const float base = slope2 * static_cast<float>(j0 - ic);
+            float2 bias[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              bias[q] = make_float2(fmaf(slope2, static_cast<float>(2 * q), base),
+                                    fmaf(slope2, static_cast<float>(2 * q + 1), base));
+            const float2 step = make_float2(8.f * slope2, 8.f * slope2);
+#pragma unroll
+            for (int c = 0; c < kHalfCols; c += 2) {
+              const int q = (c >> 1) & 3;
+              const float2 v = ptx::fma2(make_float2(x[c], x[c + 1]), cl, bias[q]);
+              bias[q] = ptx::add2(bias[q], step);
+              x[c] = v.x;
+              x[c + 1] = v.y;
+            }
+          }
+          float mx[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mx[e] = fmaxf(x[e], x[4 + e]);
+#pragma unroll
+          for (int c = 8; c < kHalfCols; c += 8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx[e] = ptx::max3(mx[e], x[c + e], x[c + 4 + e]);
+          const float tm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+#pragma unroll
+          for (int b = 0; b < NBLK; ++b) cmax[b] = tm;
+          row_done = true;
+        }
         // Score transform and max, 32 columns at a time: the first block
         // while the others are still being read from TMEM.
 #pragma unroll
-        for (int hf = 0; hf < NBLK && !sc_fast; ++hf) {
+        for (int hf = 0; hf < NBLK && !row_done; ++hf) {
           const int c0 = hf * 32;
           if (hf == 1 && !loads_done) {
             ptx::tmem_ld_wait();
