@@ -113,14 +113,14 @@ struct EmuPairs {
   static_assert(value >= 0 && value <= 16, "share of FMA-pipe exponentials");
 };
 
-// Optionally (FL_PINGPONG=1), in units where both slots walk the same key
-// tiles, the two slots' exponent phases take turns: a slot waits for the
-// other slot's previous phase to end, so that each slot's loads, maxima and
-// waits overlap the other slot's exponentials.  It only orders work: the
-// wait gives up quietly after kTurnWaitNs.  The MUFU unit of sm_103a
-// sustains about 32 ex2 per clock per SM, enough for both slots at once, and
-// the turns cost more than they save on the score-modified variants: off by
-// default.
+// In units where both slots walk the same key tiles, the two slots'
+// exponent phases can take turns: a slot waits for the other slot's previous
+// phase to end, so that each slot's loads, maxima and waits overlap the other
+// slot's exponentials.  It only orders work: the wait gives up quietly after
+// kTurnWaitNs.  Left alone, the slots' phases drift into lockstep within a
+// few tiles and then contend for the MUFU unit; the turns pay off only where
+// the transform phase is long (softcap), so they are on for softcap and,
+// with FL_PINGPONG=1, for every score_mod.
 #ifndef FL_PINGPONG
 #define FL_PINGPONG 0
 #endif
@@ -913,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t scnt = 0, uc = 0, it = 0;
     uint32_t kscnt = 0;  // slot 0: key-split merges done so far
     uint32_t pc = 0;  // P tiles handed to the MMA warp so far (= P V launched for this slot)
-    constexpr bool kPingPong = kPerSlot && FL_PINGPONG;
+    constexpr bool kPingPong = kPerSlot && (FL_PINGPONG || SCORE == SCORE_SOFTCAP);
     uint32_t tcnt = 0;  // exponent phases taken in turns so far
     bool ok = true;
 
