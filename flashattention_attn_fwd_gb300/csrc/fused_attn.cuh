@@ -126,7 +126,7 @@ struct EmuPairs {
 #endif
 constexpr uint64_t kTurnWaitNs = 1500;
 
-template <int D, int DV, int KIND>
+template <int D, int DV, int KIND, int SCORE = SCORE_NONE>
 struct Layout {
   static_assert(D == 32 || D == 64 || D == 128, "head dim");
   static_assert(DV == 32 || DV == 64 || DV == 128, "value head dim");
@@ -156,7 +156,14 @@ struct Layout {
   static constexpr int UNIT_BYTES = 128;
   static constexpr int XCH_BYTES = KIND == KIND_DIFF ? 2 * kBlockM * 4 : 0;     // differential: row sums
   static constexpr int XM_BYTES = kRowSplit == 2 ? 12 * kBlockM * 4 : 0;         // two threads per row
-  static constexpr int FIXED_BYTES = 64 * 8 + 64 + XCH_BYTES + 4 * UNIT_BYTES + XM_BYTES;
+  // ALiBi on the tensor core: one extra k-step of the S product, with a
+  // constant key-index tile K_ext [128 keys][16] and per slot a one-row
+  // tile Q_ext [8 rows][16] (read for all 128 rows) holding slope / scale
+  // split into three bf16 parts; both K-major without swizzle.
+  static constexpr bool EXT = KIND == KIND_ATTN && SCORE == SCORE_ALIBI;
+  static constexpr int EXTK_BYTES = EXT ? kBlockN * 32 : 0;
+  static constexpr int EXTQ_BYTES = EXT ? 4 * 256 : 0;  // [Q buffer][slot]
+  static constexpr int FIXED_BYTES = 64 * 8 + 64 + XCH_BYTES + 4 * UNIT_BYTES + XM_BYTES + EXTK_BYTES + EXTQ_BYTES;
   static constexpr int BUDGET = 227 * 1024 - 1024 - FIXED_BYTES;
   // Q is double-buffered (the next unit's Q loads while this one runs) when
   // that still leaves room for two stages.
@@ -180,7 +187,11 @@ struct Layout {
   static constexpr int OFF_UNITS = OFF_XCH + XCH_BYTES;        // Unit[4]: decoded units, ring
   static constexpr int OFF_XMAX = OFF_UNITS + 4 * UNIT_BYTES;   // float [2 parities][2 slots][2 halves][128]
   static constexpr int OFF_XL = OFF_XMAX + 8 * kBlockM * 4;     // float [2 slots][2 halves][128]
-  static constexpr int END = OFF_XMAX + XM_BYTES;
+  // Q_ext[buffer][slot] (256 bytes each), then K_ext; every address either
+  // descriptor can form stays inside these 5 KB
+  static constexpr int OFF_EXTQ = OFF_XMAX + XM_BYTES;
+  static constexpr int OFF_EXTK = OFF_EXTQ + EXTQ_BYTES;
+  static constexpr int END = OFF_EXTK + EXTK_BYTES;
   // +1 KB to align the dynamic base to 1024; at least ~117 KB so that only
   // one block (which owns all 512 TMEM columns) is resident per SM.
   static constexpr int SMEM_BYTES = (END + 1024) > 120 * 1024 ? (END + 1024) : 120 * 1024;
@@ -515,13 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmO,
                           const __grid_constant__ CUtensorMap tmPB, const __grid_constant__ CUtensorMap tmMB,
                           const __grid_constant__ KParams p) {
-  using L = Layout<D, DV, KIND>;
+  using L = Layout<D, DV, KIND, SCORE>;
   constexpr int S = L::STAGES;
   constexpr bool kEvo = KIND == KIND_EVO || KIND == KIND_EVO_COL;
   // TMEM columns: S0 [0,128) S1 [128,256); with DV <= 64 a separate P region
   // P0 [256,320) P1 [320,384) and O0, O1 from 384; with DV = 128 P is
   // written over the first 64 columns of S and O0, O1 start at 256.
   constexpr bool kSepP = DV <= 64;
+  // ALiBi's bias enters S through one extra k-step (see Layout::EXT)
+  constexpr bool kAlibiExt = L::EXT;
   constexpr uint32_t kColP = kSepP ? 256u : 0u;   // + 64 * slot (sep) or + 128 * slot (aliased)
   constexpr uint32_t kColO = kSepP ? 384u : 256u;
   // per-slot key ranges need one MMA thread per slot
@@ -597,6 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&misc[0], 512);
     ptx::tmem_relinquish();
   }
+  if (kAlibiExt && threadIdx.x < kBlockN) {
+    // K_ext row c: channels 0..2 hold the key index c within its tile (exact
+    // in bf16), the rest zero; 8-row core matrices of 16-byte rows, the two
+    // channel halves 128 bytes apart, row groups 256 bytes apart
+    const int c = threadIdx.x;
+    uint8_t* row = smem + L::OFF_EXTK + (c >> 3) * 256 + (c & 7) * 16;
+    const float fc = static_cast<float>(c);
+    *reinterpret_cast<uint4*>(row) = make_uint4(ptx::pack_bf16x2(fc, fc), ptx::pack_bf16x2(fc, 0.f), 0u, 0u);
+    *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+  }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&tmQ0); ptx::prefetch_tensormap(&tmK0); ptx::prefetch_tensormap(&tmV);
     ptx::prefetch_tensormap(&tmO);
@@ -635,6 +659,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
           const int qi = static_cast<int>(qb) * 2 + s;
           if (!wait_bar(&q_empty[qi], qph ^ 1u, ctl, 1)) { ok = false; break; }
+          if (kAlibiExt) {
+            // Q_ext of this slot: a = slope / scale as three bf16 parts
+            // (a = h1 + h2 + h3 to within 2^-24 relative), the same in all 8
+            // rows of the core matrix that every row group reads
+            const float a = __ldg(p.slopes + U.hq[s]) / p.scale;
+            const float h1 = __bfloat162float(__float2bfloat16_rn(a));
+            const float h2 = __bfloat162float(__float2bfloat16_rn(a - h1));
+            const float h3 = __bfloat162float(__float2bfloat16_rn(a - h1 - h2));
+            const uint4 w = make_uint4(ptx::pack_bf16x2(h1, h2), ptx::pack_bf16x2(h3, 0.f), 0u, 0u);
+            uint8_t* qe = smem + L::OFF_EXTQ + qi * 256;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              *reinterpret_cast<uint4*>(qe + 16 * i) = w;
+              *reinterpret_cast<uint4*>(qe + 128 + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            ptx::fence_proxy_async_smem();
+          }
           ptx::mbar_arrive_expect_tx(&q_full[qi], L::Q_BYTES);
           const CUtensorMap* mq = (KIND == KIND_DIFF && s == 1) ? &tmQ1 : &tmQ0;
 #pragma unroll
@@ -722,6 +763,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q_base = ptx::smem_u32(smem + L::OFF_Q);
     const uint32_t k_base = ptx::smem_u32(smem + L::OFF_K);
     const uint32_t v_base = ptx::smem_u32(smem + L::OFF_V);
+    const uint32_t qext_base = ptx::smem_u32(smem + L::OFF_EXTQ);
+    const uint32_t kext_base = ptx::smem_u32(smem + L::OFF_EXTK);
     uint32_t sf[2] = {0u, 0u};
 
     // Descriptors are built once per call from the tile base; the k-step
@@ -738,6 +781,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < D / 16; ++kb) {
         const uint32_t off = ((kb * 16 / L::BOXW_D) * L::BOX_D_BYTES + (kb * 16 % L::BOXW_D) * 2) >> 4;
         ptx::mma_ss(tmem + s * 128, ad0 + off, bd0 + off, IDESC_S, kb > 0 ? 1u : 0u);
+      }
+      if (kAlibiExt) {
+        // + (slope / scale) * (key index in the tile), no swizzle, K-major:
+        // core matrices 128 bytes apart along k; Q_ext's row groups all
+        // alias one core matrix (stride 0), K_ext's are 256 bytes apart
+        const uint64_t qe = ptx::smem_desc(qext_base + (qb * 2 + s) * 256, 128, 0, 0u);
+        const uint64_t ke = ptx::smem_desc(kext_base, 128, 256, 0u);
+        ptx::mma_ss(tmem + s * 128, qe, ke, IDESC_S, 1u);
       }
       ptx::mma_commit(&s_full[s]);
       ++sf[s];
@@ -904,11 +955,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(smem + L::OFF_XMAX);   // [parity][slot][half][row]
     float* xl = reinterpret_cast<float*>(smem + L::OFF_XL);       // [slot][half][row]
     const float scale_log2 = p.scale_log2;
-    // Scores stay in the units of the transform until the exponent:
-    // raw q.k (plain scores: the scale is folded into the exponent's FMA),
-    // natural units (Evoformer: scale q.k + biases), log2 units otherwise.
+    // Scores stay in the units of the transform until the exponent: raw S
+    // (plain scores, and ALiBi, whose column term comes with S: the scale is
+    // folded into the exponent's FMA), natural units (Evoformer: scale q.k +
+    // biases), log2 units otherwise (softcap).
     constexpr bool kRaw = SCORE == SCORE_NONE && !kEvo;
-    const float xmul = kRaw ? scale_log2 : (kEvo ? kLog2e : 1.0f);
+    const float xmul = (kRaw || kAlibiExt) ? scale_log2 : (kEvo ? kLog2e : 1.0f);
     constexpr int kEmu = EmuPairs<KIND, SCORE>::value;
     uint32_t scnt = 0, uc = 0, it = 0;
     uint32_t kscnt = 0;  // slot 0: key-split merges done so far
@@ -1314,8 +1366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < NBLK; ++b) cmax[b] = tm;
           }
         }
-        // ALiBi and plain scores on such a tile: the same whole-row form (one
-        // straight-line transform and max tree instead of four blocks)
+        // ALiBi (its bias already in S) and plain scores on such a tile: the
+        // same whole-row form (one max tree instead of four blocks)
         if ((SCORE == SCORE_ALIBI || kRaw) && !tile_part) {
           ptx::tmem_ld_wait();
 #pragma unroll
@@ -1324,24 +1376,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&s_free[s]);
           loads_done = true;
-          if (SCORE == SCORE_ALIBI) {
-            const float2 cl = make_float2(scale_log2, scale_log2);
-            const float base = slope2 * static_cast<float>(j0 - ic);
-            float2 bias[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              bias[q] = make_float2(fmaf(slope2, static_cast<float>(2 * q), base),
-                                    fmaf(slope2, static_cast<float>(2 * q + 1), base));
-            const float2 step = make_float2(8.f * slope2, 8.f * slope2);
-#pragma unroll
-            for (int c = 0; c < kHalfCols; c += 2) {
-              const int q = (c >> 1) & 3;
-              const float2 v = ptx::fma2(make_float2(x[c], x[c + 1]), cl, bias[q]);
-              bias[q] = ptx::add2(bias[q], step);
-              x[c] = v.x;
-              x[c + 1] = v.y;
-            }
-          }
           float mx[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) mx[e] = fmaxf(x[e], x[4 + e]);
@@ -1368,27 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s_free[s]);
           }
-          if (SCORE == SCORE_ALIBI) {
-            // x = s * scale_log2 + slope_log2 * (j - i); the bias of columns
-            // (c, c+1) is kept in four running pairs, each advanced by 8
-            // columns: no per-column constants
-            const float2 cl = make_float2(scale_log2, scale_log2);
-            const float base = slope2 * static_cast<float>(j0 + c0 - ic);
-            float2 bias[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              bias[q] = make_float2(fmaf(slope2, static_cast<float>(2 * q), base),
-                                    fmaf(slope2, static_cast<float>(2 * q + 1), base));
-            const float2 step = make_float2(8.f * slope2, 8.f * slope2);
-#pragma unroll
-            for (int c = c0; c < c0 + 32; c += 2) {
-              const int q = (c >> 1) & 3;
-              const float2 v = ptx::fma2(make_float2(x[c], x[c + 1]), cl, bias[q]);
-              bias[q] = ptx::add2(bias[q], step);
-              x[c] = v.x;
-              x[c + 1] = v.y;
-            }
-          } else if (SCORE == SCORE_SOFTCAP) {
+          if (SCORE == SCORE_SOFTCAP) {
             // x = cap*log2(e) * tanh(s * scale / cap): an odd polynomial in
             // s on the FMA pipe when every |s| of the warp's block is within
             // its range, else the exact form 1 - 2 / (1 + e^(2y)).
@@ -1476,7 +1490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           rmax = fmaxf(rmax, xmax[((par * 2 + s) * 2 + (half ^ 1)) * kBlockM + r]);
         }
         if (tr) FL_TR(2 + s, scnt, 2);
-        const float tmax = rmax * xmul;
+        // ALiBi: the row's term slope * (j0 - i) of this tile, in log2 units
+        const float dlt = kAlibiExt ? slope2 * static_cast<float>(j0 - ic) : 0.f;
+        const float tmax = rmax * xmul + dlt;
         // raise the reference max only when the tile's max exceeds it by more
         // than the threshold (or it is the first finite max of the row);
         // alpha = 2^(m_old - m_new) is 0 when m_old = -inf
@@ -1506,7 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exponentials and the row sum; P is packed to bf16 pairs in
         // registers while this slot's previous P V may still be reading P
         const float msub = (m == -CUDART_INF_F) ? 0.f : m;
-        const float2 negm = make_float2(-msub, -msub);
+        const float2 negm = make_float2(dlt - msub, dlt - msub);
         const float2 xm2 = make_float2(xmul, xmul);
         float2 ls[2];
         ls[0] = ls[1] = make_float2(0.f, 0.f);

@@ -9,7 +9,7 @@ namespace fl {
 template <int D, int DV, int KIND, int SCORE>
 cudaError_t launch_fused(const CUtensorMap* maps, const KParams& p, int grid, cudaStream_t stream) {
   auto kern = fused_attn_fwd_kernel<D, DV, KIND, SCORE>;
-  constexpr int smem = Layout<D, DV, KIND>::SMEM_BYTES;
+  constexpr int smem = Layout<D, DV, KIND, SCORE>::SMEM_BYTES;
   // The register split (setmaxnreg) hands the control warpgroup's registers
   // to the softmax warpgroups; it needs exactly kLaunchRegs per thread at
   // launch, or the softmax warpgroups would wait for registers forever.
