@@ -179,8 +179,8 @@ struct Layout {
   static constexpr int OFF_BAR = OFF_MB + STAGES * MB_BYTES;
   // barriers: q_full[4] q_empty[4] kv_full[S] kv_empty[S] s_full[2] s_free[2]
   //           p_full[2] pv_done[2] o_empty[2] drain[2] xch_full[1] stagger[1]
-  //           o_staged[2] xm_bar[8] xl_bar[8] exp_turn[2] ks_full[1]
-  static constexpr int NBARS = 43 + 2 * STAGES;
+  //           o_staged[2] xm_bar[8] xl_bar[8] exp_turn[2] ks_full[1] p_hi[2]
+  static constexpr int NBARS = 45 + 2 * STAGES;
   static_assert(NBARS <= 64, "barrier area");
   static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int OFF_XCH = OFF_MISC + 64;                // float [2][128]
@@ -535,6 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kSepP = DV <= 64;
   // ALiBi's bias enters S through one extra k-step (see Layout::EXT)
   constexpr bool kAlibiExt = L::EXT;
+  // P handed to the tensor core in two halves of 64 keys: the first half's
+  // P V runs while the softmax warps compute the second half's exponentials
+  constexpr bool kSplitP = kSepP && kRowSplit == 1;
   constexpr uint32_t kColP = kSepP ? 256u : 0u;   // + 64 * slot (sep) or + 128 * slot (aliased)
   constexpr uint32_t kColO = kSepP ? 384u : 256u;
   // per-slot key ranges need one MMA thread per slot
@@ -560,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xl_bar = bars + 32 + 2 * S;    // [slot * 4 + quad]: half-row sums exchanged
   uint64_t* exp_turn = bars + 40 + 2 * S;  // [slot]: the other slot's exponent phase is over
   uint64_t* ks_full = bars + 42 + 2 * S;   // key-split unit: slot 1's (m, l) published
+  uint64_t* p_hi = bars + 43 + 2 * S;      // [slot]: P of the tile's upper 64 keys in TMEM (kSplitP)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   float* xch = reinterpret_cast<float*>(smem + L::OFF_XCH);
   // The TMA thread decodes each unit once and publishes it here before
@@ -602,6 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&exp_turn[0], kSoftmaxWarps / 2);
     ptx::mbar_init(&exp_turn[1], kSoftmaxWarps / 2);
     ptx::mbar_init(ks_full, kSoftmaxWarps / 2);
+    ptx::mbar_init(&p_hi[0], kSoftmaxWarps / 2);
+    ptx::mbar_init(&p_hi[1], kSoftmaxWarps / 2);
     misc[1] = 0u;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -794,13 +800,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++sf[s];
       return true;
     };
-    auto issue_pv = [&](int s, int st, bool acc) {
+    auto issue_pv = [&](int s, int st, bool acc, int kb0 = 0, int kb1 = kBlockN / 16) {
       const uint32_t va = v_base + (st * L::NV + (L::NV == 2 ? s : 0)) * L::V_BYTES;
       const uint64_t bd0 = ptx::smem_desc(va, L::BOX_V_BYTES, 8 * L::ROWB_V, L::SWZ_V);
       const uint32_t tP = tmem + (kSepP ? kColP + s * 64 : s * 128);
       const uint32_t tO = tmem + kColO + s * DV;
 #pragma unroll
-      for (int kb = 0; kb < kBlockN / 16; ++kb)
+      for (int kb = kb0; kb < kb1; ++kb)
         ptx::mma_ts(tO, tP + kb * 8, bd0 + ((kb * 16 * L::ROWB_V) >> 4), IDESC_O, (acc || kb > 0) ? 1u : 0u);
     };
     auto wait_q = [&](uint32_t ucn, int s) -> bool {
@@ -849,11 +855,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           FL_TR(s, idx, 2);
           if (k == 0 && !wait_bar(&o_empty[s], (uc & 1u) ^ 1u, ctl, 13)) { ok = false; break; }
-          if (!wait_bar(&p_full[s], pc & 1u, ctl, 14)) { ok = false; break; }
+          const uint32_t pph = pc & 1u;
+          if (!wait_bar(&p_full[s], pph, ctl, 14)) { ok = false; break; }
           FL_TR(s, idx, 4);
           ++pc;
           ptx::tc_fence_after();
-          issue_pv(s, st, k > 0);
+          if (kSplitP) {
+            issue_pv(s, st, k > 0, 0, kBlockN / 32);
+            if (!wait_bar(&p_hi[s], pph, ctl, 16)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv(s, st, true, kBlockN / 32, kBlockN / 16);
+          } else {
+            issue_pv(s, st, k > 0);
+          }
           ptx::mma_commit(&pv_done[s]);
           ptx::mma_commit(&kv_empty[st]);
           if (k + 1 == ns && kCross && un < sch.end) {
@@ -1527,8 +1541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 ls[2];
         ls[0] = ls[1] = make_float2(0.f, 0.f);
         uint32_t pk[kHalfCols / 2];
-#pragma unroll
-        for (int h = 0; h < kHalfCols / 32; ++h) {
+        // exponentials of 32-column block h: P packed to bf16 pairs, row sum
+        auto expb = [&](int h) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 xv = make_float2(x[h * 32 + 2 * e], x[h * 32 + 2 * e + 1]);
@@ -1542,14 +1556,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ls[e & 1] = ptx::add2(ls[e & 1], pv);
             pk[h * 16 + e] = ptx::pack_bf16x2(pv.x, pv.y);
           }
+        };
+        // blocks before the P hand-over (all of them unless P goes in halves)
+        constexpr int NB1 = kSplitP ? NBLK / 2 : NBLK;
+#pragma unroll
+        for (int h = 0; h < NB1; ++h) expb(h);
+        if (!kSplitP) {
+          if (turns) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&exp_turn[s ^ 1]);
+            ++tcnt;
+          }
+          const float2 lsum = ptx::add2(ls[0], ls[1]);
+          l += lsum.x + lsum.y;
         }
-        if (turns) {
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&exp_turn[s ^ 1]);
-          ++tcnt;
-        }
-        const float2 lsum = ptx::add2(ls[0], ls[1]);
-        l += lsum.x + lsum.y;
         if (tr) FL_TR(2 + s, scnt, 4);
         // the previous P V of this slot must be done before P (and O) change
         if (pc > 0 && !__all_sync(0xffffffffu, wait_bar(&pv_done[s], (pc - 1) & 1u, ctl, 24 + s))) {
@@ -1558,7 +1578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < kHalfCols / 32; ++h)
+        for (int h = 0; h < NB1; ++h)
           ptx::tmem_st16(tP + h * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[h * 16]));
         if (tr) FL_TR(2 + s, scnt, 5);
         // O rescale (this thread's half of the columns) after the P stores
@@ -1587,6 +1607,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&p_full[s]);
+        if (kSplitP) {
+          // the upper 64 keys while the tensor core takes the lower ones
+#pragma unroll
+          for (int h = NB1; h < NBLK; ++h) expb(h);
+          if (turns) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&exp_turn[s ^ 1]);
+            ++tcnt;
+          }
+          const float2 lsum = ptx::add2(ls[0], ls[1]);
+          l += lsum.x + lsum.y;
+#pragma unroll
+          for (int h = NB1; h < NBLK; ++h)
+            ptx::tmem_st16(tP + h * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[h * 16]));
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&p_hi[s]);
+        }
         if (tr) FL_TR(2 + s, scnt, 6);
         ++pc;
       }
