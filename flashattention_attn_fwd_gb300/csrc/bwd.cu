@@ -270,9 +270,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = 0; c < 128; c += 32) ptx::reg_fence32f(&x[c]);
       const float slope2 = SCORE == SCORE_ALIBI ? __ldg(p.slopes + h) * kLog2e : 0.f;
       const bool any_vis = __any_sync(0xffffffffu, cqlo <= i0 + 127 && cqhi >= i0);
-      // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs
+      // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs (the
+      // query rows' L2 read four at a time)
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
+      for (int c4 = 0; c4 < 128; c4 += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(l2 + c4);
+        const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+        const int c = c4 + e4;
         float t;
         if (SCORE == SCORE_SOFTCAP) {
           const float kcap = p.softcap * kLog2e;
@@ -285,7 +291,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         const int q = i0 + c;
         const bool vis = any_vis && q >= cqlo && q <= cqhi;
-        x[c] = vis ? ptx::ex2(t - l2[c]) : 0.f;
+        x[c] = vis ? ptx::ex2(t - lq[e4]) : 0.f;
+        }
       }
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
@@ -312,11 +319,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tmem_ld_wait();
         ptx::reg_fence32f(dpv);
         if (SCORE == SCORE_SOFTCAP) ptx::reg_fence32f(sv);
+        float dv32[32];  // D of the 32 query rows, four at a time
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c + 4 * w);
+          dv32[4 * w] = d4.x; dv32[4 * w + 1] = d4.y; dv32[4 * w + 2] = d4.z; dv32[4 * w + 3] = d4.w;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float d0 = x[c + e] * (dpv[e] - dvec[c + e]);
-          float d1 = x[c + e + 1] * (dpv[e + 1] - dvec[c + e + 1]);
+          float d0 = x[c + e] * (dpv[e] - dv32[e]);
+          float d1 = x[c + e + 1] * (dpv[e + 1] - dv32[e + 1]);
           if (SCORE == SCORE_SOFTCAP) {
             const float th0 = tanhf(sv[e] * p.scale / p.softcap), th1 = tanhf(sv[e + 1] * p.scale / p.softcap);
             d0 *= 1.0f - th0 * th0;
