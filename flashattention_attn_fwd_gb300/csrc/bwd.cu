@@ -189,23 +189,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t ID_DQ = ptx::idesc_bf16_f32(128, D, true) | (1u << 15);  // dQ: A = dS, M-major
       const uint32_t k_a = ptx::smem_u32(smem + L::OFF_K), v_a = ptx::smem_u32(smem + L::OFF_V);
       const uint32_t ds_a = ptx::smem_u32(smem + L::OFF_DS);
-      bool ok = n_tiles == 0 || wait_bar(kv_full, 0u, ctl, 51);
-      for (int n = 0; n < n_tiles && ok; ++n) {
+      const uint64_t dsa = ptx::smem_desc(ds_a, 128 * 128, 1024, 2u);
+      const uint64_t kn = ptx::smem_desc(k_a, L::TILE, 8 * L::ROWB, L::SWZ);
+      const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::ROWB, L::SWZ);
+      const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::ROWB, L::SWZ);
+      // S^T = K Q^T and dP^T = V dO^T of query tile n (K-major, k-steps of 16
+      // channels), each once its Q / dO tile has landed
+      auto issue_s = [&](int n) -> bool {
         const int buf = n & 1;
-        const uint32_t ph = n & 1;
-        if (!wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 52)) { ok = false; break; }
+        if (!wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 52)) return false;
         ptx::tc_fence_after();
-        const uint32_t q_a = ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE);
-        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + buf * L::TILE);
-        // S^T = K Q^T and dP^T = V dO^T (both K-major, k-steps of 16 channels)
-        const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::ROWB, L::SWZ), qb = ptx::smem_desc(q_a, 16, 8 * L::ROWB, L::SWZ);
-        const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::ROWB, L::SWZ), dob = ptx::smem_desc(do_a, 16, 8 * L::ROWB, L::SWZ);
+        const uint64_t qb = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE), 16, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColS, ka + kb * 2, qb + kb * 2, ID_SS, kb > 0);
         ptx::mma_commit(s_full);
+        return true;
+      };
+      auto issue_dp = [&](int n) {
+        const uint64_t dob =
+            ptx::smem_desc(ptx::smem_u32(smem + L::OFF_DO + (n & 1) * L::TILE), 16, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColDP, va + kb * 2, dob + kb * 2, ID_SS, kb > 0);
         ptx::mma_commit(dp_full);
+      };
+      // The products of tile n + 1 are issued as soon as the compute warps
+      // are done with the TMEM they overwrite, so that the next P and dS find
+      // them ready: S^T(n+1) right after dV(n) (softcap: after dS(n), which
+      // reads S^T again), dP^T(n+1) right after dK(n).  One thread's MMAs run
+      // in issue order, so dV(n) has read P^T and dK(n) dS^T before the next
+      // products overwrite those columns, and a commit covers every product
+      // issued before it.
+      bool ok = n_tiles == 0 || (wait_bar(kv_full, 0u, ctl, 51) && issue_s(0));
+      if (ok && n_tiles > 0) issue_dp(0);
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        const int buf = n & 1;
+        const uint32_t ph = n & 1;
+        const bool more = n + 1 < n_tiles;
+        const uint32_t q_a = ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE);
+        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + buf * L::TILE);
         // dV += P^T dO (B = dO as [queries][D], N contiguous)
         if (!wait_bar(p_full, ph, ctl, 53)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -213,17 +234,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ts(tmem + kColDV, tmem + kColP + kb * 8, don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
-        // dK += dS^T Q, then dQ = dS K once the previous dQ has been read
+        if (SCORE != SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
+        // dK += dS^T Q
         if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint64_t qn = ptx::smem_desc(q_a, L::TILE, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8, qn + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
+        if (SCORE == SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
+        if (more) issue_dp(n + 1);
+        // dQ = dS K once the dQ warps have read the previous one
         if (!wait_bar(dq_free, ph ^ 1u, ctl, 55)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint64_t dsa = ptx::smem_desc(ds_a, 128 * 128, 1024, 2u);
-        const uint64_t kn = ptx::smem_desc(k_a, L::TILE, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ss(tmem + kColDQ, dsa + ((kb * 16 * 128) >> 4), kn + ((kb * 16 * L::ROWB) >> 4), ID_DQ, kb > 0);
