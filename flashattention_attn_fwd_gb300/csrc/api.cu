@@ -508,9 +508,15 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
   p.window = d.window; p.prefix = d.prefix_len; p.num_docs = d.num_docs;
   if (static_cast<int64_t>(d.B) * d.Hkv * p.n_ktiles > 0x7fffffff) return FL_ERR_UNSUPPORTED;
-  CUtensorMap maps[6];
+  CUtensorMap maps[7];
   const int bw = box_width(d.d);
   const int64_t sl = d.d;
+  // the fp32 dQ accumulator as [B * Hq][Lq][d], boxes of 32 channels x 128
+  // rows (the target of the kernel's bulk reductions)
+  const uint64_t qa_dims[3] = {static_cast<uint64_t>(d.d), static_cast<uint64_t>(d.Lq),
+                               static_cast<uint64_t>(d.B) * d.Hq};
+  const uint64_t qa_str[2] = {static_cast<uint64_t>(d.d) * 4, static_cast<uint64_t>(d.Lq) * d.d * 4};
+  const uint32_t qa_box[3] = {32u, 128u, 1u};
   if (!encode_bhlc(&maps[0], q, d.d, d.Lq, d.Hq, d.B, sl, static_cast<int64_t>(d.Lq) * d.d,
                    static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
       !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sl, static_cast<int64_t>(d.Lk) * d.d,
@@ -520,7 +526,9 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
       !encode_bhlc(&maps[3], dout, d.d, d.Lq, d.Hq, d.B, sl, static_cast<int64_t>(d.Lq) * d.d,
                    static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
       !encode_rows_f32(&maps[4], p.l2, static_cast<int64_t>(d.B) * d.Hq, d.Lq) ||
-      !encode_rows_f32(&maps[5], p.dvec, static_cast<int64_t>(d.B) * d.Hq, d.Lq))
+      !encode_rows_f32(&maps[5], p.dvec, static_cast<int64_t>(d.B) * d.Hq, d.Lq) ||
+      !encode(&maps[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.dq_acc, qa_dims, qa_str, qa_box,
+              CU_TENSOR_MAP_SWIZZLE_128B))
     return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
   return launched("backward kernel launch", fl::launch_bwd(d.d, d.score_mod, maps, p, static_cast<cudaStream_t>(d.stream)));
 }

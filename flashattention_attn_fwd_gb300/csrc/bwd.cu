@@ -23,7 +23,9 @@
 //   dQ   = dS K    (A = dS smem, M-major; B = K)    TMEM [320+2D,320+3D)
 // Warp roles (384 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-7
 // compute P and dS (one thread per key row), warps 8-11 add dQ into the
-// accumulator (one thread per query row).  Every wait is bounded.
+// accumulator (one thread per query row): they stage the fp32 tile in shared
+// memory and one thread adds it to global memory with a TMA bulk reduction.
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,7 +52,9 @@ struct BwdLayout {
   static constexpr int OFF_Q = 2 * TILE;               // Q[2]
   static constexpr int OFF_DO = 4 * TILE;              // dO[2]
   static constexpr int OFF_DS = 6 * TILE;              // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
-  static constexpr int OFF_VEC = OFF_DS + 2 * 128 * 128;  // fp32 L2[2][128], Dv[2][128]
+  static constexpr int DQS = 128 * D * 4;              // one fp32 dQ tile: D / 32 boxes [128 rows][32], 128B swizzle
+  static constexpr int OFF_DQS = OFF_DS + 2 * 128 * 128;  // dQ staging [2]
+  static constexpr int OFF_VEC = OFF_DQS + 2 * DQS;    // fp32 L2[2][128], Dv[2][128]
   static constexpr int OFF_BAR = OFF_VEC + 4 * 128 * 4;
   static constexpr int NBARS = 16;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmDv,
-                    const __grid_constant__ BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   constexpr uint32_t kColS = 0, kColP = 128, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
   extern __shared__ uint8_t bsm_raw[];
@@ -408,14 +412,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
   } else {
     // ------------------------------------------- dQ accumulation (query rows)
+    // Per tile: TMEM -> registers (then dQ's TMEM is free again), registers ->
+    // staging buffer n & 1 (swizzled: row r's 16-byte chunk k at k ^ (r & 7)),
+    // and one thread adds the staged tile to the fp32 accumulator with a bulk
+    // tensor reduction (rows past Lq skipped by the map).  Whether to go on is
+    // decided jointly by the four warps (barrier with an AND), so that every
+    // warp takes the same named barriers.
     ptx::setmaxnreg_inc<kSoftmaxRegs>();
     const int quad = warp & 3;
     const int r = quad * 32 + lane;          // query row of the tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool issuer = warp == 8 && lane == 0;
+    constexpr uint32_t kBarDQ = 1, kDQThreads = 128;
     bool ok = true;
     for (int n = 0; n < n_tiles && ok; ++n) {
       const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
-      if (!__all_sync(0xffffffffu, wait_bar(dq_full, n & 1u, ctl, 70))) { ok = false; break; }
+      const bool got = __all_sync(0xffffffffu, wait_bar(dq_full, n & 1u, ctl, 70));
+      if (!ptx::named_bar_and(kBarDQ, kDQThreads, got)) { ok = false; break; }
       ptx::tc_fence_after();
       float a[D];
 #pragma unroll
@@ -426,52 +439,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(dq_free);
-      if (i0 + r < p.Lq) {
-        float* dst = p.dq_acc + ((static_cast<int64_t>(b) * p.Hq + h) * p.Lq + i0 + r) * D;
+      // the reduction issued two tiles ago has read this buffer
+      if (issuer) ptx::bulk_wait_group_read1();
+      ptx::named_bar_sync(kBarDQ, kDQThreads);
+      uint8_t* sb = smem + L::OFF_DQS + (n & 1) * L::DQS;
 #pragma unroll
-        for (int c = 0; c < D; c += 4)
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c), "f"(a[c]), "f"(a[c + 1]),
-                       "f"(a[c + 2]), "f"(a[c + 3])
-                       : "memory");
+      for (int c = 0; c < D; c += 4)
+        *reinterpret_cast<float4*>(sb + (c >> 5) * (128 * 128) + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4)) =
+            make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(kBarDQ, kDQThreads);
+      if (issuer) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) ptx::tma_reduce_add_3d(&tmDQ, sb + bx * (128 * 128), 32 * bx, i0, b * p.Hq + h);
+        ptx::bulk_commit_group();
       }
     }
+    if (issuer) ptx::bulk_wait_group0();
     ptx::tc_fence_before();
     __syncthreads();
   }
 }
 
 // D_i = sum_c dO_ic O_ic, L2_i = LSE_i log2(e) (a row that saw no key:
-// +inf, so that its P is 0), and the dQ accumulator zeroed; one warp per row.
+// +inf, so that its P is 0), and the dQ accumulator zeroed; D / 8 lanes per
+// row, 16 bytes of O and dO each.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= p.rows) return;
-  constexpr int PER = D / 32;
-  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + row * D + lane * PER;
-  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * PER;
+  constexpr int LPR = D / 8;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (256 / LPR) + threadIdx.x / LPR;
+  const int sub = threadIdx.x % LPR;
+  const bool valid = row < p.rows;
+  const int64_t off = (valid ? row : 0) * D + sub * 8;
+  const uint4 ov = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.out) + off));
+  const uint4 gv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off));
+  const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
   float s = 0.f;
 #pragma unroll
-  for (int c = 0; c < PER; ++c) s = fmaf(__bfloat162float(o[c]), __bfloat162float(g[c]), s);
+  for (int c = 0; c < 4; ++c) {
+    const float2 of = __bfloat1622float2(o2[c]), gf = __bfloat1622float2(g2[c]);
+    s = fmaf(of.x, gf.x, fmaf(of.y, gf.y, s));
+  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  float* acc = p.dq_acc + row * D + lane * PER;
-#pragma unroll
-  for (int c = 0; c < PER; ++c) acc[c] = 0.f;
-  if (lane == 0) {
+  for (int w = LPR / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+  if (!valid) return;
+  float4* acc = reinterpret_cast<float4*>(p.dq_acc + off);
+  acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (sub == 0) {
     p.dvec[row] = s;
     const float l = p.lse[row];
     p.l2[row] = l == -CUDART_INF_F ? CUDART_INF_F : l * kLog2e;
   }
 }
 
-// dQ = scale * accumulator, rounded to bf16.
+// dQ = scale * accumulator, rounded to bf16; eight elements per thread.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constant__ BwdParams p) {
-  const int64_t e = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
+  const int64_t e = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
   if (e >= p.rows * D) return;
-  reinterpret_cast<__nv_bfloat162*>(p.dq)[e / 2] =
-      __floats2bfloat162_rn(p.dq_acc[e] * p.scale, p.dq_acc[e + 1] * p.scale);
+  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + e);
+  const float4 c = *reinterpret_cast<const float4*>(p.dq_acc + e + 4);
+  const float f = p.scale;
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + e) =
+      make_uint4(ptx::pack_bf16x2(a.x * f, a.y * f), ptx::pack_bf16x2(a.z * f, a.w * f),
+                 ptx::pack_bf16x2(c.x * f, c.y * f), ptx::pack_bf16x2(c.z * f, c.w * f));
 }
 
 template <int D, int SCORE>
@@ -486,14 +519,14 @@ cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStrea
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   }();
   if (checked != cudaSuccess) return checked;
-  const int rgrid = static_cast<int>((p.rows + 7) / 8);
+  const int rgrid = static_cast<int>((p.rows + 256 / (D / 8) - 1) / (256 / (D / 8)));
   attn_bwd_pre_kernel<D><<<rgrid, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kern<<<p.B * p.Hkv * p.n_ktiles, kBwdThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  kern<<<p.B * p.Hkv * p.n_ktiles, kBwdThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int pgrid = static_cast<int>((p.rows * D / 2 + 255) / 256);
+  const int pgrid = static_cast<int>((p.rows * D / 8 + 255) / 256);
   attn_bwd_post_kernel<D><<<pgrid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
