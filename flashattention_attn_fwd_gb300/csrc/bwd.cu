@@ -17,21 +17,23 @@
 //   S^T  = K Q^T   (A = K smem, B = Q smem)         TMEM [0,128)
 //   P^T  (bf16, written by the compute warps)        TMEM [128,192)
 //   dP^T = V dO^T  (A = V smem, B = dO smem)        TMEM [192,320)
-//   dS^T (bf16, over the first half of dP^T)         TMEM [192,256)
+//   dS^T (bf16; queries 0-63 over dP^T's [192,224), 64-127 over [256,288))
 //   dV  += P^T dO  (A = P^T TMEM, B = dO smem)      TMEM [320,320+D)
 //   dK  += dS^T Q  (A = dS^T TMEM, B = Q smem)      TMEM [320+D,320+2D)
 //   dQ   = dS K    (A = dS smem, M-major; B = K)    TMEM [320+2D,320+3D)
-// Warp roles (384 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-7
-// compute P and dS (one thread per key row), warps 8-11 add dQ into the
-// accumulator (one thread per query row): they stage the fp32 tile in shared
-// memory and one thread adds it to global memory with a TMA bulk reduction.
-// Every wait is bounded.
+// Warp roles (512 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-11
+// compute P and dS (one thread per key row and half of the query columns:
+// two warps per scheduler), warps 12-15 add dQ into the accumulator (one
+// thread per query row): they stage the fp32 tile in shared memory and one
+// thread adds it to global memory with a TMA bulk reduction.  Every wait is
+// bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "bwd.h"
 #include "fused_attn.cuh"
@@ -39,7 +41,12 @@
 namespace fl {
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
+// registers: 128 per thread at launch, then 56 (TMA / MMA warps), 168 (P and
+// dS), 120 (dQ) -- together exactly the launch's 512 x 128
+constexpr int kBwdLaunchRegs = 128, kBwdCtlRegs = 56, kBwdComputeRegs = 168, kBwdDQRegs = 120;
+static_assert(128 * kBwdCtlRegs + 256 * kBwdComputeRegs + 128 * kBwdDQRegs <= kBwdThreads * kBwdLaunchRegs,
+              "backward register split");
 
 template <int D>
 struct BwdLayout {
@@ -138,8 +145,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(p_full, 4);
-    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(p_full, 8);
+    ptx::mbar_init(ds_full, 8);
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 4);
     ptx::mbar_init(done, 1);
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint64_t drain_ns = 50ull * 1000ull * 1000ull;
 
   if (warp < 4) {
-    ptx::setmaxnreg_dec<kCtlRegs>();
+    ptx::setmaxnreg_dec<kBwdCtlRegs>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- TMA
       const uint64_t pol_keep = ptx::policy_evict_last();
@@ -239,13 +246,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ts(tmem + kColDV, tmem + kColP + kb * 8, don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
         if (SCORE != SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
-        // dK += dS^T Q
+        // dK += dS^T Q (dS^T of queries 64-127 sits 64 columns further on)
         if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint64_t qn = ptx::smem_desc(q_a, L::TILE, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8, qn + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
+          ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8 + (kb >= 4 ? 32 : 0), qn + ((kb * 16 * L::ROWB) >> 4),
+                      ID_ACC, (n > 0 || kb > 0));
         if (SCORE == SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
         if (more) issue_dp(n + 1);
         // dQ = dS K once the dQ warps have read the previous one
@@ -267,112 +275,146 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_after();
       ptx::tmem_dealloc(tmem, 512);
     }
-  } else if (warp < 8) {
-    // -------------------------------------------------- P and dS (key rows)
-    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+  } else if (warp < 12) {
+    // ---------------------------------------- P and dS (key rows, half tiles)
+    // Thread (quad, lane) of half hf owns key row r and the query columns
+    // [64 hf, 64 hf + 64) of every query tile: its S^T, P^T and dP^T columns.
+    ptx::setmaxnreg_inc<kBwdComputeRegs>();
     const int quad = warp & 3;
+    const int hf = (warp - 4) >> 2;
     const int r = quad * 32 + lane;          // key row of the tile
     const int kg = j0 + r;                   // key index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t cS = kColS + 64 * hf;     // S^T (softcap: then sech^2 of the score, fp32)
+    const uint32_t cP = kColP + 32 * hf;     // P^T, bf16 pairs
+    const uint32_t cDP = kColDP + 64 * hf;   // dP^T; dS^T as bf16 pairs over its first 32 columns
     int cqlo, cqhi;
     col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
     if (kg >= p.Lk) { cqlo = 1; cqhi = 0; }  // keys past the end see nothing
     const float scale_log2 = p.scale * kLog2e;
+    const float kcap = p.softcap * kLog2e;
+    const float zmul = SCORE == SCORE_SOFTCAP ? 2.0f * scale_log2 / p.softcap : 0.f;
     bool ok = true;
     for (int n = 0; n < n_tiles && ok; ++n) {
       const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
+      const int q0 = i0 + 64 * hf;           // first query column of this half
       const int buf = n & 1;
       const uint32_t ph = n & 1;
-      const float* l2 = vec + buf * 128;
-      const float* dvec = vec + 256 + buf * 128;
+      const float* l2 = vec + buf * 128 + 64 * hf;
+      const float* dvec = vec + 256 + buf * 128 + 64 * hf;
       if (!__all_sync(0xffffffffu, wait_bar(s_full, ph, ctl, 60))) { ok = false; break; }
       // this tile's LSE and D rows came with Q (TMA); observe that barrier too
       if (!__all_sync(0xffffffffu, wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 64))) { ok = false; break; }
       ptx::tc_fence_after();
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) ptx::tmem_ld32f(tl + kColS + c, &x[c]);
+      float x[64];
+      ptx::tmem_ld32f(tl + cS, &x[0]);
+      ptx::tmem_ld32f(tl + cS + 32, &x[32]);
       ptx::tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) ptx::reg_fence32f(&x[c]);
+      ptx::reg_fence32f(&x[0]);
+      ptx::reg_fence32f(&x[32]);
       const float slope2 = SCORE == SCORE_ALIBI ? __ldg(p.slopes + h) * kLog2e : 0.f;
-      const bool any_vis = __any_sync(0xffffffffu, cqlo <= i0 + 127 && cqhi >= i0);
-      // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs (the
-      // query rows' L2 read four at a time)
+      // ALiBi: slope2 (k - q) = abase - slope2 c for query q0 + c
+      const float abase = slope2 * static_cast<float>(kg - q0);
+      // the warp's rows all see all 64 columns (no per-element test), or some
+      const bool all_vis = __all_sync(0xffffffffu, cqlo <= q0 && cqhi >= q0 + 63);
+      const bool any_vis = __any_sync(0xffffffffu, cqlo <= q0 + 63 && cqhi >= q0);
+      // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs; softcap also
+      // leaves sech^2(s / cap) = 4 d (1 - d), d = 1 / (1 + e^(2 s / cap)), in
+      // the S^T columns for the dS step (nothing reads S^T again before the
+      // next tile's S^T, which is issued after this tile's dS)
+      auto p_chunk = [&](int c0, auto full) {
+        uint32_t sech[32];  // fp32 bits
 #pragma unroll
-      for (int c4 = 0; c4 < 128; c4 += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(l2 + c4);
-        const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c4 = 0; c4 < 32; c4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(l2 + c0 + c4);
+          const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-        const int c = c4 + e4;
-        float t;
-        if (SCORE == SCORE_SOFTCAP) {
-          const float kcap = p.softcap * kLog2e;
-          const float ez = ptx::ex2(x[c] * (2.0f * scale_log2 / p.softcap));
-          t = fmaf(-2.0f * kcap, ptx::rcp(1.0f + ez), kcap);
-        } else if (SCORE == SCORE_ALIBI) {
-          t = fmaf(x[c], scale_log2, slope2 * static_cast<float>(kg - (i0 + c)));
-        } else {
-          t = x[c] * scale_log2;
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const int c = c0 + c4 + e4;
+            float t;
+            if (SCORE == SCORE_SOFTCAP) {
+              const float dd = ptx::rcp(1.0f + ptx::ex2(x[c] * zmul));
+              t = fmaf(-2.0f * kcap, dd, kcap);
+              sech[c4 + e4] = __float_as_uint(4.0f * dd * (1.0f - dd));
+            } else if (SCORE == SCORE_ALIBI) {
+              t = fmaf(x[c], scale_log2, fmaf(-slope2, static_cast<float>(c), abase));
+            } else {
+              t = x[c] * scale_log2;
+            }
+            if (decltype(full)::value) {
+              x[c] = ptx::ex2(t - lq[e4]);
+            } else {
+              const int q = q0 + c;
+              x[c] = any_vis && q >= cqlo && q <= cqhi ? ptx::ex2(t - lq[e4]) : 0.f;
+            }
+          }
         }
-        const int q = i0 + c;
-        const bool vis = any_vis && q >= cqlo && q <= cqhi;
-        x[c] = vis ? ptx::ex2(t - lq[e4]) : 0.f;
-        }
+        if (SCORE == SCORE_SOFTCAP) ptx::tmem_st32(tl + cS + c0, sech);
+      };
+      if (all_vis) {
+        p_chunk(0, std::true_type{});
+        p_chunk(32, std::true_type{});
+      } else {
+        p_chunk(0, std::false_type{});
+        p_chunk(32, std::false_type{});
       }
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = ptx::pack_bf16x2(x[c + 2 * e], x[c + 2 * e + 1]);
-        ptx::tmem_st16(tl + kColP + c / 2, pk);
+        ptx::tmem_st16(tl + cP + c / 2, pk);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_full);
-      // dS^T = P^T (dP^T - D_q) (* 1 - tanh^2 for softcap), 32 columns at a time
+      // dS^T = P^T (dP^T - D_q) (* sech^2 for softcap)
       if (!__all_sync(0xffffffffu, wait_bar(dp_full, ph, ctl, 61))) { ok = false; break; }
       // the previous dQ product must have read the dS tile in shared memory
       if (n > 0 && !__all_sync(0xffffffffu, wait_bar(dq_full, ph ^ 1u, ctl, 62))) { ok = false; break; }
       ptx::tc_fence_after();
+      float dpv[64];
+      ptx::tmem_ld32f(tl + cDP, &dpv[0]);
+      if (SCORE != SCORE_SOFTCAP) ptx::tmem_ld32f(tl + cDP + 32, &dpv[32]);
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        float dpv[32];
-        ptx::tmem_ld32f(tl + kColDP + c, dpv);
+      for (int c = 0; c < 64; c += 32) {
         float sv[32];
-        if (SCORE == SCORE_SOFTCAP) ptx::tmem_ld32f(tl + kColS + c, sv);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32f(dpv);
-        if (SCORE == SCORE_SOFTCAP) ptx::reg_fence32f(sv);
-        float dv32[32];  // D of the 32 query rows, four at a time
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c + 4 * w);
-          dv32[4 * w] = d4.x; dv32[4 * w + 1] = d4.y; dv32[4 * w + 2] = d4.z; dv32[4 * w + 3] = d4.w;
+        if (SCORE == SCORE_SOFTCAP) {
+          if (c > 0) ptx::tmem_ld32f(tl + cDP + c, &dpv[c]);
+          ptx::tmem_ld32f(tl + cS + c, sv);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32f(sv);
+          ptx::reg_fence32f(&dpv[c]);
+        } else if (c == 0) {
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32f(&dpv[0]);
+          ptx::reg_fence32f(&dpv[32]);
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float d0 = x[c + e] * (dpv[e] - dv32[e]);
-          float d1 = x[c + e + 1] * (dpv[e + 1] - dv32[e + 1]);
-          if (SCORE == SCORE_SOFTCAP) {
-            const float th0 = tanhf(sv[e] * p.scale / p.softcap), th1 = tanhf(sv[e + 1] * p.scale / p.softcap);
-            d0 *= 1.0f - th0 * th0;
-            d1 *= 1.0f - th1 * th1;
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c + e4);
+          const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            float d0 = x[c + e4 + e] * (dpv[c + e4 + e] - dq4[e]);
+            float d1 = x[c + e4 + e + 1] * (dpv[c + e4 + e + 1] - dq4[e + 1]);
+            if (SCORE == SCORE_SOFTCAP) {
+              d0 *= sv[e4 + e];
+              d1 *= sv[e4 + e + 1];
+            }
+            pk[(e4 + e) / 2] = ptx::pack_bf16x2(d0, d1);
           }
-          pk[e / 2] = ptx::pack_bf16x2(d0, d1);
         }
-        // dS^T over the first half of the dP^T columns (already read) ...
-        ptx::tmem_st16(tl + kColDP + c / 2, pk);
-        // ... and dS into shared memory: row r (key) of two [128][64] boxes,
-        // 16-byte chunks at the 128-byte swizzle positions
+        // dS^T over the first half of this half's dP^T columns (already read) ...
+        ptx::tmem_st16(tl + cDP + c / 2, pk);
+        // ... and dS into shared memory: row r (key) of box hf ([128][64],
+        // 16-byte chunks at the 128-byte swizzle positions)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const int qc = c + 8 * w;                      // first query column of this chunk
-          const int bx = qc >> 6, chunk = (qc & 63) >> 3;
-          *reinterpret_cast<uint4*>(smem + L::OFF_DS + bx * 128 * 128 + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+          const int chunk = (c >> 3) + w;
+          *reinterpret_cast<uint4*>(smem + L::OFF_DS + hf * 128 * 128 + r * 128 + ((chunk ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
         }
       }
@@ -382,30 +424,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ds_full);
     }
-    // dK, dV of this thread's key row, once every product is done (the
-    // TMEM loads are warp-wide; only the stores depend on the row)
+    // dV (half 0) or dK (half 1) of this thread's key row, once every product
+    // is done (the TMEM loads are warp-wide; only the stores depend on the row)
     if (ok && __all_sync(0xffffffffu, wait_bar(done, 0u, ctl, 63))) {
       ptx::tc_fence_after();
       const int64_t roff = ((static_cast<int64_t>(b) * p.Hkv + hkv) * p.Lk + kg) * D;
+      float a[D];
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        float a[D];
+      for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + (hf ? kColDK : kColDV) + c, &a[c]);
+      ptx::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + (which ? kColDK : kColDV) + c, &a[c]);
-        ptx::tmem_ld_wait();
+      for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
+      const float f = (hf && n_tiles > 0) ? p.scale : 1.0f;
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hf ? p.dk : p.dv) + roff);
+      if (kg < p.Lk) {
+        const bool z = n_tiles == 0;
 #pragma unroll
-        for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
-        const float f = (which && n_tiles > 0) ? p.scale : 1.0f;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + roff);
-        if (kg >= p.Lk) continue;
-#pragma unroll
-        for (int c = 0; c < D; c += 8) {
-          const bool z = n_tiles == 0;
+        for (int c = 0; c < D; c += 8)
           dst[c / 8] = make_uint4(ptx::pack_bf16x2(z ? 0.f : a[c] * f, z ? 0.f : a[c + 1] * f),
                                   ptx::pack_bf16x2(z ? 0.f : a[c + 2] * f, z ? 0.f : a[c + 3] * f),
                                   ptx::pack_bf16x2(z ? 0.f : a[c + 4] * f, z ? 0.f : a[c + 5] * f),
                                   ptx::pack_bf16x2(z ? 0.f : a[c + 6] * f, z ? 0.f : a[c + 7] * f));
-        }
       }
     }
     ptx::tc_fence_before();
@@ -418,11 +457,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // tensor reduction (rows past Lq skipped by the map).  Whether to go on is
     // decided jointly by the four warps (barrier with an AND), so that every
     // warp takes the same named barriers.
-    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    ptx::setmaxnreg_dec<kBwdDQRegs>();
     const int quad = warp & 3;
     const int r = quad * 32 + lane;          // query row of the tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool issuer = warp == 8 && lane == 0;
+    const bool issuer = warp == 12 && lane == 0;
     constexpr uint32_t kBarDQ = 1, kDQThreads = 128;
     bool ok = true;
     for (int n = 0; n < n_tiles && ok; ++n) {
@@ -515,7 +554,7 @@ cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStrea
     cudaFuncAttributes a{};
     cudaError_t e = cudaFuncGetAttributes(&a, kern);
     if (e != cudaSuccess) return e;
-    if (a.numRegs != kLaunchRegs) return cudaErrorInvalidDeviceFunction;
+    if (a.numRegs != kBwdLaunchRegs) return cudaErrorInvalidDeviceFunction;
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   }();
   if (checked != cudaSuccess) return checked;
