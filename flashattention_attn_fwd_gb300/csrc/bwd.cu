@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
     if (kg >= p.Lk) { cqlo = 1; cqhi = 0; }  // keys past the end see nothing
     const float scale_log2 = p.scale * kLog2e;
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
     const float kcap = p.softcap * kLog2e;
     const float zmul = SCORE == SCORE_SOFTCAP ? 2.0f * scale_log2 / p.softcap : 0.f;
     bool ok = true;
@@ -327,25 +328,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 32; c4 += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(l2 + c0 + c4);
-          const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const int c = c0 + c4 + e4;
-            float t;
+          for (int e2 = 0; e2 < 4; e2 += 2) {
+            const int c = c0 + c4 + e2;
+            const float2 lq = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+            const float2 xv = make_float2(x[c], x[c + 1]);
+            float2 arg;  // t log2 e - L2_q of the pair
             if (SCORE == SCORE_SOFTCAP) {
-              const float dd = ptx::rcp(1.0f + ptx::ex2(x[c] * zmul));
-              t = fmaf(-2.0f * kcap, dd, kcap);
-              sech[c4 + e4] = __float_as_uint(4.0f * dd * (1.0f - dd));
+              const float d0 = ptx::rcp(1.0f + ptx::ex2(xv.x * zmul));
+              const float d1 = ptx::rcp(1.0f + ptx::ex2(xv.y * zmul));
+              arg = make_float2(fmaf(-2.0f * kcap, d0, kcap) - lq.x, fmaf(-2.0f * kcap, d1, kcap) - lq.y);
+              sech[c4 + e2] = __float_as_uint(4.0f * d0 * (1.0f - d0));
+              sech[c4 + e2 + 1] = __float_as_uint(4.0f * d1 * (1.0f - d1));
             } else if (SCORE == SCORE_ALIBI) {
-              t = fmaf(x[c], scale_log2, fmaf(-slope2, static_cast<float>(c), abase));
+              arg = ptx::fma2(xv, sc2,
+                              make_float2(fmaf(-slope2, static_cast<float>(c), abase) - lq.x,
+                                          fmaf(-slope2, static_cast<float>(c + 1), abase) - lq.y));
             } else {
-              t = x[c] * scale_log2;
+              arg = ptx::fma2(xv, sc2, make_float2(-lq.x, -lq.y));
             }
+            const float2 pv = make_float2(ptx::ex2(arg.x), ptx::ex2(arg.y));
             if (decltype(full)::value) {
-              x[c] = ptx::ex2(t - lq[e4]);
+              x[c] = pv.x;
+              x[c + 1] = pv.y;
             } else {
               const int q = q0 + c;
-              x[c] = any_vis && q >= cqlo && q <= cqhi ? ptx::ex2(t - lq[e4]) : 0.f;
+              x[c] = any_vis && q >= cqlo && q <= cqhi ? pv.x : 0.f;
+              x[c + 1] = any_vis && q + 1 >= cqlo && q + 1 <= cqhi ? pv.y : 0.f;
             }
           }
         }
