@@ -157,11 +157,20 @@ def make_calls(api, bufs, slopes):
     return calls
 
 
-def kernel_source_hash():
+# Each kernel family is built from every source file except the ones only
+# another family uses, so a change to (say) the backward leaves the forward
+# kernels' counters valid.
+KERNEL_FAMILY_EXCLUDES = {"forward": ("bwd.", "decode."), "backward": ("decode.",), "decode": ("bwd.",)}
+TRAFFIC_FAMILY = {"decode": "decode", "backward": "backward"}  # every other entry: forward
+
+
+def kernel_source_hash(family="forward"):
+    """Hash of the sources one kernel family is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flashattention_attn_fwd_gb300", "csrc")
+    skip = KERNEL_FAMILY_EXCLUDES[family]
     for f in sorted(os.listdir(csrc)):
-        if not f.endswith((".cu", ".cuh", ".h")):
+        if not f.endswith((".cu", ".cuh", ".h")) or f.startswith(skip):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
@@ -170,14 +179,15 @@ def kernel_source_hash():
 
 def ncu_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel's family; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             tr = json.load(f)
     except (OSError, ValueError):
         return None
-    if tr.get("source_hash") != kernel_source_hash():
+    fam = TRAFFIC_FAMILY.get(kernel_key, "forward")
+    if tr.get("source_hashes", {}).get(fam) != kernel_source_hash(fam):
         return None
     ent = tr.get("kernels", {}).get(kernel_key)
     return None if ent is None else ent.get("dram_bytes_per_launch")

@@ -88,3 +88,28 @@ def test_autograd_function_matches_oracle():
     _cmp(qd.grad, rq, "dq")
     _cmp(kd.grad, rk, "dk")
     _cmp(vd.grad, rv, "dv")
+
+
+# The benchmark's backward workload at full size (B=4 H=16 L=2048 d=64,
+# causal; the same seeds and the same launch configuration the benchmark
+# times), plus softcap 30.  Heads are independent (Hq = Hkv), so the oracle's
+# exact gradients of a sampled (b, h) slice are those of the whole problem
+# restricted to that head; three heads spread over the grid's key-tile-major
+# CTA order are compared under the bar above.
+@pytest.mark.parametrize("kw", [dict(mask="causal"), dict(mask="causal", score_mod="softcap", softcap=30.0)],
+                         ids=["causal", "causal-softcap30"])
+def test_bwd_fullsize_sampled_heads(kw):
+    B, H, L, d = 4, 16, 2048, 64
+    q, k, v = synth.attn_inputs(B, H, H, L, d, seed=90)
+    dout = synth.randn_bf16((B, H, L, d), synth.generator(91))
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    out, lse = attn_fwd(qd, kd, vd, **kw)
+    dq, dk, dv = attn_bwd(qd, kd, vd, out, dod, lse, **kw)
+    sync_status()
+    okw = {k_: v_ for k_, v_ in kw.items()}
+    for b, h in ((0, 0), (1, 7), (3, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        rq, rk, rv = oracle.attention_backward(q[sl], k[sl], v[sl], dout[sl], **okw)
+        _cmp(dq[sl], rq, f"dq[{b},{h}]")
+        _cmp(dk[sl], rk, f"dk[{b},{h}]")
+        _cmp(dv[sl], rv, f"dv[{b},{h}]")
