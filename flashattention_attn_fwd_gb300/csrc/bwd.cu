@@ -60,8 +60,9 @@ struct BwdLayout {
   static constexpr int OFF_DO = 4 * TILE;              // dO[2]
   static constexpr int OFF_DS = 6 * TILE;              // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
   static constexpr int DQS = 128 * D * 4;              // one fp32 dQ tile: D / 32 boxes [128 rows][32], 128B swizzle
-  static constexpr int OFF_DQS = OFF_DS + 2 * 128 * 128;  // dQ staging [2]
-  static constexpr int OFF_VEC = OFF_DQS + 2 * DQS;    // fp32 L2[2][128], Dv[2][128]
+  static constexpr int OFF_DQS = OFF_DS + 2 * 128 * 128;  // dQ staging (the previous tile's reduction
+                                                          // has a whole tile period to read it out)
+  static constexpr int OFF_VEC = OFF_DQS + DQS;        // fp32 L2[2][128], Dv[2][128]
   static constexpr int OFF_BAR = OFF_VEC + 4 * 128 * 4;
   static constexpr int NBARS = 16;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------- dQ accumulation (query rows)
     // Per tile: TMEM -> registers (then dQ's TMEM is free again), registers ->
-    // staging buffer n & 1 (swizzled: row r's 16-byte chunk k at k ^ (r & 7)),
+    // the staging buffer (swizzled: row r's 16-byte chunk k at k ^ (r & 7)),
     // and one thread adds the staged tile to the fp32 accumulator with a bulk
     // tensor reduction (rows past Lq skipped by the map).  Whether to go on is
     // decided jointly by the four warps (barrier with an AND), so that every
@@ -487,10 +488,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(dq_free);
-      // the reduction issued two tiles ago has read this buffer
-      if (issuer) ptx::bulk_wait_group_read1();
+      // the previous tile's reduction has read the staging buffer
+      if (issuer) ptx::bulk_wait_group_read0();
       ptx::named_bar_sync(kBarDQ, kDQThreads);
-      uint8_t* sb = smem + L::OFF_DQS + (n & 1) * L::DQS;
+      uint8_t* sb = smem + L::OFF_DQS;
 #pragma unroll
       for (int c = 0; c < D; c += 4)
         *reinterpret_cast<float4*>(sb + (c >> 5) * (128 * 128) + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4)) =
