@@ -39,6 +39,10 @@ CFG = [
     ("2c-window256", 4, 16, 16, 2048, dict(mask="window", window=256)),
     ("3a-gqa-doc8", 2, 32, 8, 8192, dict(mask="document")),
     ("3b-gqa-prefix1024", 2, 32, 8, 8192, dict(mask="prefix_lm", prefix=1024)),
+    # the longest sequence of the pages' range (16k), causal softcap and a
+    # long GQA window
+    ("16k-causal-softcap30", 1, 8, 8, 16384, dict(mask="causal", score_mod="softcap", softcap=30.0)),
+    ("16k-gqa-window4096", 1, 16, 4, 16384, dict(mask="window", window=4096)),
 ]
 
 
