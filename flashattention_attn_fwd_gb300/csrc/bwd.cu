@@ -14,13 +14,17 @@
 // dK and dV stay in TMEM for the whole walk, and each query tile's dQ
 // contribution is added to an fp32 accumulator in global memory.  All five
 // products run on tcgen05 with accumulators in TMEM:
-//   S^T  = K Q^T   (A = K smem, B = Q smem)         TMEM [0,128)
+//   S^T  = K Q^T   (A = K, B = Q smem)              TMEM [0,128)
 //   P^T  (bf16, written by the compute warps)        TMEM [128,192)
 //   dP^T = V dO^T  (A = V smem, B = dO smem)        TMEM [192,320)
 //   dS^T (bf16; queries 0-63 over dP^T's [192,224), 64-127 over [256,288))
 //   dV  += P^T dO  (A = P^T TMEM, B = dO smem)      TMEM [320,320+D)
 //   dK  += dS^T Q  (A = dS^T TMEM, B = Q smem)      TMEM [320+D,320+2D)
 //   dQ   = dS K    (A = dS smem, M-major; B = K)    TMEM [320+2D,320+3D)
+// Without softcap, P^T goes over the first half of each half-tile's S^T
+// columns instead, and K and V (constant over the walk) sit in TMEM
+// [128,192) as the A operands of S^T and dP^T, which then read only Q and
+// dO from shared memory (its bandwidth is what the products contend for).
 // Warp roles (512 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-11
 // compute P and dS (one thread per key row and half of the query columns:
 // two warps per scheduler), warps 12-15 add dQ into the accumulator (one
@@ -104,6 +108,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   constexpr uint32_t kColS = 0, kColP = 128, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
+  // no softcap: P^T over S^T, K and V in TMEM (softcap keeps sech^2 in S^T)
+  constexpr bool kKVT = SCORE != SCORE_SOFTCAP;
+  constexpr uint32_t kColKT = 128, kColVT = 128 + D / 2;
   extern __shared__ uint8_t bsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dq_full = bars + 9;
   uint64_t* dq_free = bars + 10;
   uint64_t* done = bars + 11;
+  uint64_t* kvt_ready = bars + 12;  // K and V copied into TMEM
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // L2[buf][128] then Dv[buf][128]
 
@@ -151,6 +159,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 4);
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(kvt_ready, 8);
     misc[1] = 0u;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -213,7 +222,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tc_fence_after();
         const uint64_t qb = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE), 16, 8 * L::ROWB, L::SWZ);
 #pragma unroll
-        for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColS, ka + kb * 2, qb + kb * 2, ID_SS, kb > 0);
+        for (int kb = 0; kb < D / 16; ++kb) {
+          if (kKVT) ptx::mma_ts(tmem + kColS, tmem + kColKT + kb * 8, qb + kb * 2, ID_SS, kb > 0);
+          else ptx::mma_ss(tmem + kColS, ka + kb * 2, qb + kb * 2, ID_SS, kb > 0);
+        }
         ptx::mma_commit(s_full);
         return true;
       };
@@ -221,7 +233,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dob =
             ptx::smem_desc(ptx::smem_u32(smem + L::OFF_DO + (n & 1) * L::TILE), 16, 8 * L::ROWB, L::SWZ);
 #pragma unroll
-        for (int kb = 0; kb < D / 16; ++kb) ptx::mma_ss(tmem + kColDP, va + kb * 2, dob + kb * 2, ID_SS, kb > 0);
+        for (int kb = 0; kb < D / 16; ++kb) {
+          if (kKVT) ptx::mma_ts(tmem + kColDP, tmem + kColVT + kb * 8, dob + kb * 2, ID_SS, kb > 0);
+          else ptx::mma_ss(tmem + kColDP, va + kb * 2, dob + kb * 2, ID_SS, kb > 0);
+        }
         ptx::mma_commit(dp_full);
       };
       // The products of tile n + 1 are issued as soon as the compute warps
@@ -231,7 +246,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // in issue order, so dV(n) has read P^T and dK(n) dS^T before the next
       // products overwrite those columns, and a commit covers every product
       // issued before it.
-      bool ok = n_tiles == 0 || (wait_bar(kv_full, 0u, ctl, 51) && issue_s(0));
+      bool ok = n_tiles == 0 ||
+                (wait_bar(kv_full, 0u, ctl, 51) && (!kKVT || wait_bar(kvt_ready, 0u, ctl, 58)) && issue_s(0));
       if (ok && n_tiles > 0) issue_dp(0);
       for (int n = 0; n < n_tiles && ok; ++n) {
         const int buf = n & 1;
@@ -245,7 +261,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t don = ptx::smem_desc(do_a, L::TILE, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDV, tmem + kColP + kb * 8, don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
+          ptx::mma_ts(tmem + kColDV, tmem + (kKVT ? kColS + kb * 8 + (kb >= 4 ? 32 : 0) : kColP + kb * 8),
+                      don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
         if (SCORE != SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
         // dK += dS^T Q (dS^T of queries 64-127 sits 64 columns further on)
         if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
@@ -287,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kg = j0 + r;                   // key index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t cS = kColS + 64 * hf;     // S^T (softcap: then sech^2 of the score, fp32)
-    const uint32_t cP = kColP + 32 * hf;     // P^T, bf16 pairs
+    const uint32_t cP = kKVT ? cS : kColP + 32 * hf;  // P^T, bf16 pairs
     const uint32_t cDP = kColDP + 64 * hf;   // dP^T; dS^T as bf16 pairs over its first 32 columns
     int cqlo, cqhi;
     col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
@@ -297,6 +314,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float kcap = p.softcap * kLog2e;
     const float zmul = SCORE == SCORE_SOFTCAP ? 2.0f * scale_log2 / p.softcap : 0.f;
     bool ok = true;
+    if (kKVT && n_tiles > 0) {
+      // this thread's key row of K (half 0) or V (half 1) into TMEM: 16-byte
+      // chunk c of row r sits at c ^ (r & 7) (128-byte rows) or
+      // c ^ ((r >> 1) & 3) (64-byte rows) of the swizzled tile
+      ok = __all_sync(0xffffffffu, wait_bar(kv_full, 0u, ctl, 65));
+      if (ok) {
+        const uint8_t* row = smem + (hf ? L::OFF_V : L::OFF_K) + r * L::ROWB;
+        uint32_t kv[D / 2];
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const int sc = L::ROWB == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+          const uint4 v4 = *reinterpret_cast<const uint4*>(row + (sc << 4));
+          kv[4 * c] = v4.x; kv[4 * c + 1] = v4.y; kv[4 * c + 2] = v4.z; kv[4 * c + 3] = v4.w;
+        }
+        const uint32_t ta = tl + (hf ? kColVT : kColKT);
+        if constexpr (D == 64) ptx::tmem_st32(ta, kv);
+        else ptx::tmem_st16(ta, kv);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(kvt_ready);
+      }
+    }
     for (int n = 0; n < n_tiles && ok; ++n) {
       const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
       const int q0 = i0 + 64 * hf;           // first query column of this half
