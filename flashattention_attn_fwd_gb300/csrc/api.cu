@@ -183,7 +183,8 @@ bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 // Softcap on the FMA pipe: cap*log2(e)*tanh(s*scale/cap) = s * Q(s^2) while
 // |s * scale / cap| <= kTanhRange (the kernel checks the range per warp).
-void softcap_coefficients(KParams& p, float scale, float cap) {
+template <class Params>
+void softcap_coefficients(Params& p, float scale, float cap) {
   const double ya = static_cast<double>(scale) / cap, k = static_cast<double>(cap) * kLog2e;
   double ypow = ya;
   for (int i = 0; i < 4; ++i) {
@@ -505,6 +506,7 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.n_ktiles = (d.Lk + 127) / 128;
   p.scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p.softcap = d.softcap;
+  if (d.score_mod == FL_SCORE_SOFTCAP) softcap_coefficients(p, p.scale, d.softcap);
   p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
   p.window = d.window; p.prefix = d.prefix_len; p.num_docs = d.num_docs;
   if (static_cast<int64_t>(d.B) * d.Hkv * p.n_ktiles > 0x7fffffff) return FL_ERR_UNSUPPORTED;

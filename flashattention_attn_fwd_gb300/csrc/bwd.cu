@@ -313,6 +313,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float2 sc2 = make_float2(scale_log2, scale_log2);
     const float kcap = p.softcap * kLog2e;
     const float zmul = SCORE == SCORE_SOFTCAP ? 2.0f * scale_log2 / p.softcap : 0.f;
+    const float2 sq0 = make_float2(p.sc_q[0], p.sc_q[0]), sq1 = make_float2(p.sc_q[1], p.sc_q[1]);
+    const float2 sq2 = make_float2(p.sc_q[2], p.sc_q[2]), sq3 = make_float2(p.sc_q[3], p.sc_q[3]);
+    const float ikc = SCORE == SCORE_SOFTCAP ? 1.0f / kcap : 0.f;
+    const float2 ikc2 = make_float2(ikc, ikc);
     bool ok = true;
     if (kKVT && n_tiles > 0) {
       // this thread's key row of K (half 0) or V (half 1) into TMEM: 16-byte
@@ -361,11 +365,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool all_vis = __all_sync(0xffffffffu, cqlo <= q0 && cqhi >= q0 + 63);
       const bool any_vis = __any_sync(0xffffffffu, cqlo <= q0 + 63 && cqhi >= q0);
       // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs; softcap also
-      // leaves sech^2(s / cap) = 4 d (1 - d), d = 1 / (1 + e^(2 s / cap)), in
-      // the S^T columns for the dS step (nothing reads S^T again before the
-      // next tile's S^T, which is issued after this tile's dS)
+      // leaves sech^2 of the scaled score over cap in the S^T columns for the
+      // dS step (nothing reads S^T again before the next tile's S^T, which is
+      // issued after this tile's dS).  When all of the warp's scores are in
+      // the polynomial's range, tanh comes from the forward's FMA-pipe
+      // polynomial (t = s q(s^2) = cap log2(e) tanh, sech^2 = 1 - tanh^2);
+      // otherwise from d = 1 / (1 + e^(2 s / cap)): tanh = 1 - 2d,
+      // sech^2 = 4 d (1 - d) (two MUFU operations more per score).
+      bool poly = false;
+      if (SCORE == SCORE_SOFTCAP) {
+        float am[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) am[c & 3] = fmaxf(am[c & 3], fabsf(x[c]));
+        poly = __all_sync(0xffffffffu, fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])) <= p.sc_smax);
+      }
       auto p_chunk = [&](int c0, auto full) {
         uint32_t sech[32];  // fp32 bits
+        if (SCORE == SCORE_SOFTCAP) {
+          // t = cap log2(e) tanh(s scale / cap) in place, and sech^2 (one
+          // form per chunk: the branch stays outside the loops)
+          if (poly) {
+#pragma unroll
+            for (int e2 = 0; e2 < 32; e2 += 2) {
+              const float2 xv = make_float2(x[c0 + e2], x[c0 + e2 + 1]);
+              const float2 z = ptx::mul2(xv, xv);
+              float2 q = ptx::fma2(sq3, z, sq2);
+              q = ptx::fma2(q, z, sq1);
+              q = ptx::fma2(q, z, sq0);
+              const float2 t = ptx::mul2(xv, q);
+              const float2 th = ptx::mul2(t, ikc2);
+              const float2 sc = ptx::fma2(make_float2(-th.x, -th.y), th, make_float2(1.0f, 1.0f));
+              x[c0 + e2] = t.x;
+              x[c0 + e2 + 1] = t.y;
+              sech[e2] = __float_as_uint(sc.x);
+              sech[e2 + 1] = __float_as_uint(sc.y);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float dd = ptx::rcp(1.0f + ptx::ex2(x[c0 + e] * zmul));
+              x[c0 + e] = fmaf(-2.0f * kcap, dd, kcap);
+              sech[e] = __float_as_uint(4.0f * dd * (1.0f - dd));
+            }
+          }
+        }
 #pragma unroll
         for (int c4 = 0; c4 < 32; c4 += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(l2 + c0 + c4);
@@ -376,11 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 xv = make_float2(x[c], x[c + 1]);
             float2 arg;  // t log2 e - L2_q of the pair
             if (SCORE == SCORE_SOFTCAP) {
-              const float d0 = ptx::rcp(1.0f + ptx::ex2(xv.x * zmul));
-              const float d1 = ptx::rcp(1.0f + ptx::ex2(xv.y * zmul));
-              arg = make_float2(fmaf(-2.0f * kcap, d0, kcap) - lq.x, fmaf(-2.0f * kcap, d1, kcap) - lq.y);
-              sech[c4 + e2] = __float_as_uint(4.0f * d0 * (1.0f - d0));
-              sech[c4 + e2 + 1] = __float_as_uint(4.0f * d1 * (1.0f - d1));
+              arg = ptx::sub2(xv, lq);  // x holds t already
             } else if (SCORE == SCORE_ALIBI) {
               arg = ptx::fma2(xv, sc2,
                               make_float2(fmaf(-slope2, static_cast<float>(c), abase) - lq.x,

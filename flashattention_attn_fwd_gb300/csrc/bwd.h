@@ -27,6 +27,10 @@ struct BwdParams {
   int n_ktiles;           // ceil(Lk / 128)
   int64_t rows;           // B * Hq * Lq
   float scale, softcap;
+  // softcap on the FMA pipe, as in the forward: cap*log2(e)*tanh(s*scale/cap)
+  // = s * (q0 + q1 s^2 + q2 s^4 + q3 s^6) while |s| <= sc_smax
+  float sc_q[4];
+  float sc_smax;
   int mask_kind, doc_causal, window, prefix, num_docs;
 };
 
