@@ -15,16 +15,17 @@
 // contribution is added to an fp32 accumulator in global memory.  All five
 // products run on tcgen05 with accumulators in TMEM:
 //   S^T  = K Q^T   (A = K, B = Q smem)              TMEM [0,128)
-//   P^T  (bf16, written by the compute warps)        TMEM [128,192)
+//   P^T  (bf16, written by the compute warps)        over S^T: [0,32), [64,96)
 //   dP^T = V dO^T  (A = V smem, B = dO smem)        TMEM [192,320)
 //   dS^T (bf16; queries 0-63 over dP^T's [192,224), 64-127 over [256,288))
 //   dV  += P^T dO  (A = P^T TMEM, B = dO smem)      TMEM [320,320+D)
 //   dK  += dS^T Q  (A = dS^T TMEM, B = Q smem)      TMEM [320+D,320+2D)
 //   dQ   = dS K    (A = dS smem, M-major; B = K)    TMEM [320+2D,320+3D)
-// Without softcap, P^T goes over the first half of each half-tile's S^T
-// columns instead, and K and V (constant over the walk) sit in TMEM
-// [128,192) as the A operands of S^T and dP^T, which then read only Q and
-// dO from shared memory (its bandwidth is what the products contend for).
+// P^T goes over the first half of each half-tile's S^T columns, so that
+// TMEM [128,192) holds either K and V (constant over the walk; the A
+// operands of S^T and dP^T, which then read only Q and dO from shared
+// memory, whose bandwidth the products contend for) or, with softcap,
+// sech^2 of the tile's scores as fp16 pairs for the dS step.
 // Warp roles (512 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-11
 // compute P and dS (one thread per key row and half of the query columns:
 // two warps per scheduler), warps 12-15 add dQ into the accumulator (one
@@ -33,6 +34,7 @@
 // bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -46,6 +48,14 @@ namespace fl {
 namespace {
 
 constexpr int kBwdThreads = 512;
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
 // registers: 128 per thread at launch, then 56 (TMA / MMA warps), 168 (P and
 // dS), 120 (dQ) -- together exactly the launch's 512 x 128
 constexpr int kBwdLaunchRegs = 128, kBwdCtlRegs = 56, kBwdComputeRegs = 168, kBwdDQRegs = 120;
@@ -107,10 +117,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmDv,
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
-  constexpr uint32_t kColS = 0, kColP = 128, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
+  constexpr uint32_t kColS = 0, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
   // no softcap: P^T over S^T, K and V in TMEM (softcap keeps sech^2 in S^T)
   constexpr bool kKVT = SCORE != SCORE_SOFTCAP;
   constexpr uint32_t kColKT = 128, kColVT = 128 + D / 2;
+  constexpr uint32_t kColSech = 128;  // softcap: sech^2, fp16 pairs, 32 columns per half
   extern __shared__ uint8_t bsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -241,11 +252,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       // The products of tile n + 1 are issued as soon as the compute warps
       // are done with the TMEM they overwrite, so that the next P and dS find
-      // them ready: S^T(n+1) right after dV(n) (softcap: after dS(n), which
-      // reads S^T again), dP^T(n+1) right after dK(n).  One thread's MMAs run
-      // in issue order, so dV(n) has read P^T and dK(n) dS^T before the next
-      // products overwrite those columns, and a commit covers every product
-      // issued before it.
+      // them ready: S^T(n+1) right after dV(n), dP^T(n+1) right after dK(n).
+      // One thread's MMAs run in issue order, so dV(n) has read P^T (over
+      // the S^T columns) and dK(n) dS^T before the next products overwrite
+      // those columns, and a commit covers every product issued before it.
       bool ok = n_tiles == 0 ||
                 (wait_bar(kv_full, 0u, ctl, 51) && (!kKVT || wait_bar(kvt_ready, 0u, ctl, 58)) && issue_s(0));
       if (ok && n_tiles > 0) issue_dp(0);
@@ -261,9 +271,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t don = ptx::smem_desc(do_a, L::TILE, 8 * L::ROWB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDV, tmem + (kKVT ? kColS + kb * 8 + (kb >= 4 ? 32 : 0) : kColP + kb * 8),
-                      don + ((kb * 16 * L::ROWB) >> 4), ID_ACC, (n > 0 || kb > 0));
-        if (SCORE != SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
+          ptx::mma_ts(tmem + kColDV, tmem + kColS + kb * 8 + (kb >= 4 ? 32 : 0), don + ((kb * 16 * L::ROWB) >> 4),
+                      ID_ACC, (n > 0 || kb > 0));
+        if (more && !issue_s(n + 1)) { ok = false; break; }
         // dK += dS^T Q (dS^T of queries 64-127 sits 64 columns further on)
         if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -272,7 +282,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8 + (kb >= 4 ? 32 : 0), qn + ((kb * 16 * L::ROWB) >> 4),
                       ID_ACC, (n > 0 || kb > 0));
-        if (SCORE == SCORE_SOFTCAP && more && !issue_s(n + 1)) { ok = false; break; }
         if (more) issue_dp(n + 1);
         // dQ = dS K once the dQ warps have read the previous one
         if (!wait_bar(dq_free, ph ^ 1u, ctl, 55)) { ok = false; break; }
@@ -303,8 +312,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = quad * 32 + lane;          // key row of the tile
     const int kg = j0 + r;                   // key index
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t cS = kColS + 64 * hf;     // S^T (softcap: then sech^2 of the score, fp32)
-    const uint32_t cP = kKVT ? cS : kColP + 32 * hf;  // P^T, bf16 pairs
+    const uint32_t cS = kColS + 64 * hf;     // S^T
+    const uint32_t cP = cS;                  // P^T, bf16 pairs, over the S^T just read
+    const uint32_t cSech = kColSech + 32 * hf;  // softcap: sech^2, fp16 pairs
     const uint32_t cDP = kColDP + 64 * hf;   // dP^T; dS^T as bf16 pairs over its first 32 columns
     int cqlo, cqhi;
     col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         poly = __all_sync(0xffffffffu, fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])) <= p.sc_smax);
       }
       auto p_chunk = [&](int c0, auto full) {
-        uint32_t sech[32];  // fp32 bits
+        uint32_t sech[16];  // fp16 pairs
         if (SCORE == SCORE_SOFTCAP) {
           // t = cap log2(e) tanh(s scale / cap) in place, and sech^2 (one
           // form per chunk: the branch stays outside the loops)
@@ -397,15 +407,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const float2 sc = ptx::fma2(make_float2(-th.x, -th.y), th, make_float2(1.0f, 1.0f));
               x[c0 + e2] = t.x;
               x[c0 + e2 + 1] = t.y;
-              sech[e2] = __float_as_uint(sc.x);
-              sech[e2 + 1] = __float_as_uint(sc.y);
+              sech[e2 >> 1] = pack_f16x2(sc.x, sc.y);
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float dd = ptx::rcp(1.0f + ptx::ex2(x[c0 + e] * zmul));
-              x[c0 + e] = fmaf(-2.0f * kcap, dd, kcap);
-              sech[e] = __float_as_uint(4.0f * dd * (1.0f - dd));
+            for (int e2 = 0; e2 < 32; e2 += 2) {
+              const float d0 = ptx::rcp(1.0f + ptx::ex2(x[c0 + e2] * zmul));
+              const float d1 = ptx::rcp(1.0f + ptx::ex2(x[c0 + e2 + 1] * zmul));
+              x[c0 + e2] = fmaf(-2.0f * kcap, d0, kcap);
+              x[c0 + e2 + 1] = fmaf(-2.0f * kcap, d1, kcap);
+              sech[e2 >> 1] = pack_f16x2(4.0f * d0 * (1.0f - d0), 4.0f * d1 * (1.0f - d1));
             }
           }
         }
@@ -438,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
         }
-        if (SCORE == SCORE_SOFTCAP) ptx::tmem_st32(tl + cS + c0, sech);
+        if (SCORE == SCORE_SOFTCAP) ptx::tmem_st16(tl + cSech + c0 / 2, sech);
       };
       if (all_vis) {
         p_chunk(0, std::true_type{});
@@ -468,12 +479,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (SCORE != SCORE_SOFTCAP) ptx::tmem_ld32f(tl + cDP + 32, &dpv[32]);
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
-        float sv[32];
+        uint32_t sv[16];  // sech^2, fp16 pairs
         if (SCORE == SCORE_SOFTCAP) {
           if (c > 0) ptx::tmem_ld32f(tl + cDP + c, &dpv[c]);
-          ptx::tmem_ld32f(tl + cS + c, sv);
+          ptx::tmem_ld16(tl + cSech + c / 2, sv);
           ptx::tmem_ld_wait();
-          ptx::reg_fence32f(sv);
+          ptx::reg_fence16(sv);
           ptx::reg_fence32f(&dpv[c]);
         } else if (c == 0) {
           ptx::tmem_ld_wait();
@@ -490,8 +501,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             float d0 = x[c + e4 + e] * (dpv[c + e4 + e] - dq4[e]);
             float d1 = x[c + e4 + e + 1] * (dpv[c + e4 + e + 1] - dq4[e + 1]);
             if (SCORE == SCORE_SOFTCAP) {
-              d0 *= sv[e4 + e];
-              d1 *= sv[e4 + e + 1];
+              const float2 sc = unpack_f16x2(sv[(e4 + e) >> 1]);
+              d0 *= sc.x;
+              d1 *= sc.y;
             }
             pk[(e4 + e) / 2] = ptx::pack_bf16x2(d0, d1);
           }
