@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   constexpr uint32_t kColS = 0, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
-  // no softcap: P^T over S^T, K and V in TMEM (softcap keeps sech^2 in S^T)
+  // TMEM [128,192): K and V without softcap, the tile's sech^2 with it
   constexpr bool kKVT = SCORE != SCORE_SOFTCAP;
   constexpr uint32_t kColKT = 128, kColVT = 128 + D / 2;
   constexpr uint32_t kColSech = 128;  // softcap: sech^2, fp16 pairs, 32 columns per half
@@ -375,9 +375,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool all_vis = __all_sync(0xffffffffu, cqlo <= q0 && cqhi >= q0 + 63);
       const bool any_vis = __any_sync(0xffffffffu, cqlo <= q0 + 63 && cqhi >= q0);
       // P^T = 2^(t log2 e - L2_q) on visible (key, query) pairs; softcap also
-      // leaves sech^2 of the scaled score over cap in the S^T columns for the
-      // dS step (nothing reads S^T again before the next tile's S^T, which is
-      // issued after this tile's dS).  When all of the warp's scores are in
+      // leaves sech^2 of the scaled score over cap (fp16 pairs, cSech) for
+      // the dS step, which the next tile's P step of these same warps
+      // overwrites only afterwards.  When all of the warp's scores are in
       // the polynomial's range, tanh comes from the forward's FMA-pipe
       // polynomial (t = s q(s^2) = cap log2(e) tanh, sech^2 = 1 - tanh^2);
       // otherwise from d = 1 / (1 + e^(2 s / cap)): tanh = 1 - 2d,
