@@ -989,6 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     struct Epi {
       uint32_t uc, pcl;  // unit counter; index of the unit's last P V completion
       float m, l;
+      int ns;            // this slot's tiles in the unit
     };
     // With two Q buffers the epilogue of a unit runs when the next unit
     // starts (its last P V completes meanwhile, and the next unit's first S
@@ -998,7 +999,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Output tile of one slot: staged in the slot's Q buffer and stored by
     // TMA when it fits (DV <= D, or half the channels for differential
     // attention), else written by each thread straight to global memory.
-    constexpr bool kTmaOut = OUT_COLS * 2 * kBlockM <= L::Q_BYTES;
+    // Evoformer row-wise (one Q buffer) stores directly instead, so that
+    // its Q buffer is free as soon as the unit's last S is done and the next
+    // unit's Q loads while this one finishes.
+    constexpr bool kTmaOut = KIND != KIND_EVO && OUT_COLS * 2 * kBlockM <= L::Q_BYTES;
+    constexpr bool kEarlyQ = !kTmaOut && KIND == KIND_EVO;
     // key-split units (attention only; the host enables them only where
     // key_split_ok holds)
     constexpr bool kKs = KIND == KIND_ATTN && key_split_ok(D, DV);
@@ -1168,8 +1173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             orow[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         }
         // this unit's Q buffer is free once both halves of every row are past
-        // their last use of it (the last S was done before the last P V)
-        if (leader) ptx::mbar_arrive(&q_empty[qi]);
+        // their last use of it (the last S was done before the last P V);
+        // released in the tile loop already when the slot had tiles
+        if (leader && (!kEarlyQ || e.ns == 0)) ptx::mbar_arrive(&q_empty[qi]);
       }
       if (tre) FL_TR(4, e.uc, 3);
       return __all_sync(0xffffffffu, !*ctl.abort);
@@ -1312,6 +1318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tr = lane == 0 && (sw == 0 || sw == 4 * kRowSplit);
         if (tr) FL_TR(2 + s, scnt, 0);
         if (!__all_sync(0xffffffffu, wait_bar(&s_full[s], scnt & 1u, ctl, 20 + s))) { ok = false; break; }
+        // the unit's last S has read this slot's Q: release the buffer
+        if (kEarlyQ && k == ns - 1 && leader) ptx::mbar_arrive(&q_empty[(uc % L::QBUF) * 2 + s]);
         if (kEvo && !__all_sync(0xffffffffu, wait_bar(&kv_full[idx % S], (idx / S) & 1u, ctl, 21))) {
           ok = false;
           break;
@@ -1633,7 +1641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       it += n;
       if (lane == 0 && sw == 0) FL_TR(4, 32 + uc, 3);
       {
-        const Epi cur{uc, pc - 1, m, l};
+        const Epi cur{uc, pc - 1, m, l, ns};
         if (kKs && Us.ks) {
           if (!epilogue_ks(cur)) {
             ok = false;
