@@ -313,6 +313,7 @@ def variant_configs():
         evo_col(),
         decode(),
         bwd("7 backward B4 H16 L2048 d64 causal", 4, 16, 2048, 64, 90, mask="causal"),
+        attn("8 d128 causal B2 H16 L4096 d128", 2, 16, 16, 4096, 128, 2, 70, mask="causal"),
     ]
 
 

@@ -64,6 +64,18 @@ def test_attn_fullsize_sampled_rows(name, B, Hq, Hkv, L, kw):
     _check_rows([oc[b, h, i].numpy() for b, h, i in rows], [lc[b, h, i].item() for b, h, i in rows], ro, rl)
 
 
+def test_attn_d128_fullsize_sampled_rows():
+    # the benchmark's head-dim-128 workload (causal, B=2 H=16 L=4096 d=128)
+    B, H, L, d = 2, 16, 4096, 128
+    q, k, v = synth.attn_inputs(B, H, H, L, d, seed=70)
+    out, lse = attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), mask="causal")
+    sync_status()
+    rows = _rows(B, H, L)
+    ro, rl = oracle.attention_rows(q, k, v, rows, mask="causal")
+    oc, lc = out.float().cpu(), lse.cpu()
+    _check_rows([oc[b, h, i].numpy() for b, h, i in rows], [lc[b, h, i].item() for b, h, i in rows], ro, rl)
+
+
 def test_diffattn_fullsize_sampled_rows():
     B, H, L = 4, 16, 4096
     q1, k1, q2, k2, v = synth.diff_inputs(B, H, L, seed=19)
