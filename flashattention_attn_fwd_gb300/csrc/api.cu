@@ -469,7 +469,7 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
   if (!desc || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FL_ERR_INVALID_ARG;
   const fl_attn_desc& d = *desc;
   if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0) return FL_ERR_INVALID_ARG;
-  if (d.d != d.dv || (d.d != 32 && d.d != 64)) return FL_ERR_UNSUPPORTED;
+  if (d.d != d.dv || (d.d != 32 && d.d != 64 && d.d != 128)) return FL_ERR_UNSUPPORTED;
   if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
   if (d.mask_kind < FL_MASK_NONE || d.mask_kind > FL_MASK_DOCUMENT) return FL_ERR_INVALID_ARG;
   if (d.mask_kind != FL_MASK_NONE && d.Lq != d.Lk) return FL_ERR_UNSUPPORTED;

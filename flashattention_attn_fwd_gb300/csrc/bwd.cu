@@ -25,7 +25,12 @@
 // TMEM [128,192) holds either K and V (constant over the walk; the A
 // operands of S^T and dP^T, which then read only Q and dO from shared
 // memory, whose bandwidth the products contend for) or, with softcap,
-// sech^2 of the tile's scores as fp16 pairs for the dS step.
+// sech^2 of the tile's scores as fp16 pairs for the dS step.  With d = 128,
+// dV and dK take 256 columns: dP^T moves to [128,256) and dQ shares those
+// columns (dP^T of the next tile waits until the dQ warps have read dQ),
+// sech^2 goes over the second half of each half-tile's S^T columns, and K, V
+// stay in shared memory, as does one dO buffer (two do not fit beside the
+// rest).
 // Warp roles (512 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-11
 // compute P and dS (one thread per key row and half of the query columns:
 // two warps per scheduler), warps 12-15 add dQ into the accumulator (one
@@ -64,16 +69,23 @@ static_assert(128 * kBwdCtlRegs + 256 * kBwdComputeRegs + 128 * kBwdDQRegs <= kB
 
 template <int D>
 struct BwdLayout {
-  static_assert(D == 32 || D == 64, "backward head dim");
+  static_assert(D == 32 || D == 64 || D == 128, "backward head dim");
   static constexpr int ROWB = D * 2;
-  static constexpr int TILE = 128 * ROWB;              // one 128-row tile of K, V, Q or dO
-  static constexpr uint32_t SWZ = ROWB == 128 ? 2u : 4u;
+  static constexpr int BOXW = D < 64 ? D : 64;         // channels per TMA box (rows of <= 128 bytes)
+  static constexpr int NBOX = D / BOXW;
+  static constexpr int BOXB = BOXW * 2;                // bytes per row of one box
+  static constexpr int BOX = 128 * BOXB;               // one box of 128 rows
+  static constexpr int TILE = NBOX * BOX;              // one 128-row tile of K, V, Q or dO
+  static constexpr uint32_t SWZ = BOXB == 128 ? 2u : 4u;
+  // d = 128: one dO buffer and one 32-channel dQ staging box; two of each
+  // would not fit in a block's 227 KB
+  static constexpr int NDO = D == 128 ? 1 : 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;               // Q[2]
-  static constexpr int OFF_DO = 4 * TILE;              // dO[2]
-  static constexpr int OFF_DS = 6 * TILE;              // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
-  static constexpr int DQS = 128 * D * 4;              // one fp32 dQ tile: D / 32 boxes [128 rows][32], 128B swizzle
+  static constexpr int OFF_DO = 4 * TILE;              // dO[NDO]
+  static constexpr int OFF_DS = OFF_DO + NDO * TILE;   // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
+  static constexpr int DQS = D == 128 ? 128 * 32 * 4 : 128 * D * 4;  // fp32 boxes [128 rows][32], 128B swizzle
   static constexpr int OFF_DQS = OFF_DS + 2 * 128 * 128;  // dQ staging (the previous tile's reduction
                                                           // has a whole tile period to read it out)
   static constexpr int OFF_VEC = OFF_DQS + DQS;        // fp32 L2[2][128], Dv[2][128]
@@ -82,6 +94,9 @@ struct BwdLayout {
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static_assert(SMEM <= 227 * 1024, "backward shared memory");
+  // k-step kb (16 channels) of a K-major tile: box kb * 16 / BOXW, 32 bytes
+  // per step within the box's 128-byte swizzled rows (descriptor units of 16 B)
+  __host__ __device__ static constexpr uint32_t koff(int kb) { return ((kb * 16 / BOXW) * BOX + (kb * 16 % BOXW) * 2) >> 4; }
 };
 
 // Queries that see key k form one interval [qlo, qhi] for every mask kind
@@ -117,11 +132,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmDv,
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
-  constexpr uint32_t kColS = 0, kColDP = 192, kColDV = 320, kColDK = 320 + D, kColDQ = 320 + 2 * D;
-  // TMEM [128,192): K and V without softcap, the tile's sech^2 with it
-  constexpr bool kKVT = SCORE != SCORE_SOFTCAP;
+  // d <= 64: S^T [0,128), K V or sech^2 [128,192), dP^T [192,320), dV, dK, dQ
+  // after.  d = 128 (dV and dK take 256 columns): S^T [0,128), dP^T [128,256)
+  // shared with dQ, dV [256,384), dK [384,512); softcap's sech^2 goes over the
+  // second half of each half-tile's S^T columns (P^T holds the first).
+  constexpr bool kWide = D == 128;
+  constexpr uint32_t kColS = 0, kColDP = kWide ? 128 : 192, kColDV = kWide ? 256 : 320;
+  constexpr uint32_t kColDK = kColDV + D, kColDQ = kWide ? kColDP : 320 + 2 * D;
+  // TMEM [128,192) (d <= 64): K and V without softcap, the tile's sech^2 with it
+  constexpr bool kKVT = SCORE != SCORE_SOFTCAP && !kWide;
   constexpr uint32_t kColKT = 128, kColVT = 128 + D / 2;
-  constexpr uint32_t kColSech = 128;  // softcap: sech^2, fp16 pairs, 32 columns per half
+  // softcap: sech^2, fp16 pairs, 32 columns per half
+  constexpr uint32_t kColSech = kWide ? 32 : 128, kSechHalf = kWide ? 64 : 32;
+  // d = 128 softcap: the next S^T overwrites sech^2, so it waits for the dS step
+  constexpr bool kLateS = kWide && SCORE == SCORE_SOFTCAP;
   extern __shared__ uint8_t bsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -136,6 +160,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dq_free = bars + 10;
   uint64_t* done = bars + 11;
   uint64_t* kvt_ready = bars + 12;  // K and V copied into TMEM
+  uint64_t* do_full = bars + 13;    // d = 128: the single dO buffer loaded ...
+  uint64_t* do_empty = bars + 14;   // ... and read by dV
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // L2[buf][128] then Dv[buf][128]
 
@@ -171,6 +197,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(dq_free, 4);
     ptx::mbar_init(done, 1);
     ptx::mbar_init(kvt_ready, 8);
+    ptx::mbar_init(do_full, 1);
+    ptx::mbar_init(do_empty, 1);
     misc[1] = 0u;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -193,26 +221,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t pol_keep = ptx::policy_evict_last();
       if (n_tiles > 0) {
         ptx::mbar_arrive_expect_tx(kv_full, 2u * L::TILE);
-        ptx::tma_load_4d(smem + L::OFF_K, &tmK, kv_full, 0, j0, hkv, b, pol_keep);
-        ptx::tma_load_4d(smem + L::OFF_V, &tmV, kv_full, 0, j0, hkv, b, pol_keep);
+#pragma unroll
+        for (int bx = 0; bx < L::NBOX; ++bx) {
+          ptx::tma_load_4d(smem + L::OFF_K + bx * L::BOX, &tmK, kv_full, bx * L::BOXW, j0, hkv, b, pol_keep);
+          ptx::tma_load_4d(smem + L::OFF_V + bx * L::BOX, &tmV, kv_full, bx * L::BOXW, j0, hkv, b, pol_keep);
+        }
       }
-      int issued = 0;
+      int issued = 0, do_issued = 0;
       bool ok = true;
       for (int n = 0; n < n_tiles && ok; ++n) {
         const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
         const int buf = n & 1;
         if (!wait_bar(&q_empty[buf], ((n >> 1) & 1u) ^ 1u, ctl, 50)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(&q_full[buf], 2u * L::TILE + 2u * 512u);
-        ptx::tma_load_4d(smem + L::OFF_Q + buf * L::TILE, &tmQ, &q_full[buf], 0, i0, h, b, pol_keep);
-        ptx::tma_load_4d(smem + L::OFF_DO + buf * L::TILE, &tmDO, &q_full[buf], 0, i0, h, b, pol_keep);
+        ptx::mbar_arrive_expect_tx(&q_full[buf], (L::NDO == 2 ? 2u : 1u) * L::TILE + 2u * 512u);
+#pragma unroll
+        for (int bx = 0; bx < L::NBOX; ++bx) {
+          ptx::tma_load_4d(smem + L::OFF_Q + buf * L::TILE + bx * L::BOX, &tmQ, &q_full[buf], bx * L::BOXW, i0, h, b,
+                           pol_keep);
+          if (L::NDO == 2)
+            ptx::tma_load_4d(smem + L::OFF_DO + buf * L::TILE + bx * L::BOX, &tmDO, &q_full[buf], bx * L::BOXW, i0,
+                             h, b, pol_keep);
+        }
         const int row = b * p.Hq + h;
         ptx::tma_load_2d(vec + buf * 128, &tmL2, &q_full[buf], i0, row, pol_keep);
         ptx::tma_load_2d(vec + 256 + buf * 128, &tmDv, &q_full[buf], i0, row, pol_keep);
         issued = n + 1;
+        if (L::NDO == 1) {
+          // one dO buffer: tile n's once dV(n - 1) has read tile n - 1's
+          if (!wait_bar(do_empty, (n & 1u) ^ 1u, ctl, 56)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(do_full, L::TILE);
+#pragma unroll
+          for (int bx = 0; bx < L::NBOX; ++bx)
+            ptx::tma_load_4d(smem + L::OFF_DO + bx * L::BOX, &tmDO, do_full, bx * L::BOXW, i0, h, b, pol_keep);
+          do_issued = n + 1;
+        }
       }
       if (*ctl.abort) {
         if (n_tiles > 0) wait_drain(kv_full, 0u, drain_ns);
         for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n) wait_drain(&q_full[n & 1], (n >> 1) & 1u, drain_ns);
+        if (do_issued > 0) wait_drain(do_full, (do_issued - 1) & 1u, drain_ns);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA
@@ -222,75 +269,92 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t k_a = ptx::smem_u32(smem + L::OFF_K), v_a = ptx::smem_u32(smem + L::OFF_V);
       const uint32_t ds_a = ptx::smem_u32(smem + L::OFF_DS);
       const uint64_t dsa = ptx::smem_desc(ds_a, 128 * 128, 1024, 2u);
-      const uint64_t kn = ptx::smem_desc(k_a, L::TILE, 8 * L::ROWB, L::SWZ);
-      const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::ROWB, L::SWZ);
-      const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::ROWB, L::SWZ);
+      // N-major B operands (N = D channels across NBOX boxes, LBO = box
+      // stride) and K-major operands (k-steps through ::koff)
+      const uint64_t kn = ptx::smem_desc(k_a, L::BOX, 8 * L::BOXB, L::SWZ);
+      const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::BOXB, L::SWZ);
+      const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::BOXB, L::SWZ);
       // S^T = K Q^T and dP^T = V dO^T of query tile n (K-major, k-steps of 16
       // channels), each once its Q / dO tile has landed
       auto issue_s = [&](int n) -> bool {
         const int buf = n & 1;
         if (!wait_bar(&q_full[buf], (n >> 1) & 1u, ctl, 52)) return false;
         ptx::tc_fence_after();
-        const uint64_t qb = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE), 16, 8 * L::ROWB, L::SWZ);
+        const uint64_t qb = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE), 16, 8 * L::BOXB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < D / 16; ++kb) {
-          if (kKVT) ptx::mma_ts(tmem + kColS, tmem + kColKT + kb * 8, qb + kb * 2, ID_SS, kb > 0);
-          else ptx::mma_ss(tmem + kColS, ka + kb * 2, qb + kb * 2, ID_SS, kb > 0);
+          if (kKVT) ptx::mma_ts(tmem + kColS, tmem + kColKT + kb * 8, qb + L::koff(kb), ID_SS, kb > 0);
+          else ptx::mma_ss(tmem + kColS, ka + L::koff(kb), qb + L::koff(kb), ID_SS, kb > 0);
         }
         ptx::mma_commit(s_full);
         return true;
       };
-      auto issue_dp = [&](int n) {
-        const uint64_t dob =
-            ptx::smem_desc(ptx::smem_u32(smem + L::OFF_DO + (n & 1) * L::TILE), 16, 8 * L::ROWB, L::SWZ);
+      auto issue_dp = [&](int n) -> bool {
+        if (L::NDO == 1) {
+          if (!wait_bar(do_full, n & 1u, ctl, 57)) return false;
+          ptx::tc_fence_after();
+        }
+        const uint64_t dob = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? (n & 1) : 0) * L::TILE),
+                                            16, 8 * L::BOXB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < D / 16; ++kb) {
-          if (kKVT) ptx::mma_ts(tmem + kColDP, tmem + kColVT + kb * 8, dob + kb * 2, ID_SS, kb > 0);
-          else ptx::mma_ss(tmem + kColDP, va + kb * 2, dob + kb * 2, ID_SS, kb > 0);
+          if (kKVT) ptx::mma_ts(tmem + kColDP, tmem + kColVT + kb * 8, dob + L::koff(kb), ID_SS, kb > 0);
+          else ptx::mma_ss(tmem + kColDP, va + L::koff(kb), dob + L::koff(kb), ID_SS, kb > 0);
         }
         ptx::mma_commit(dp_full);
+        return true;
       };
       // The products of tile n + 1 are issued as soon as the compute warps
       // are done with the TMEM they overwrite, so that the next P and dS find
-      // them ready: S^T(n+1) right after dV(n), dP^T(n+1) right after dK(n).
-      // One thread's MMAs run in issue order, so dV(n) has read P^T (over
-      // the S^T columns) and dK(n) dS^T before the next products overwrite
-      // those columns, and a commit covers every product issued before it.
+      // them ready: S^T(n+1) right after dV(n) (d = 128 softcap: after the dS
+      // step, which reads sech^2 from the S^T columns), dP^T(n+1) right after
+      // dK(n) (d = 128: once the dQ warps have read dQ(n) from the same
+      // columns).  One thread's MMAs run in issue order, so dV(n) has read P^T
+      // (over the S^T columns) and dK(n) dS^T before the next products
+      // overwrite those columns, and a commit covers every product issued
+      // before it.
       bool ok = n_tiles == 0 ||
-                (wait_bar(kv_full, 0u, ctl, 51) && (!kKVT || wait_bar(kvt_ready, 0u, ctl, 58)) && issue_s(0));
-      if (ok && n_tiles > 0) issue_dp(0);
+                (wait_bar(kv_full, 0u, ctl, 51) && (!kKVT || wait_bar(kvt_ready, 0u, ctl, 58)) && issue_s(0) &&
+                 issue_dp(0));
       for (int n = 0; n < n_tiles && ok; ++n) {
         const int buf = n & 1;
         const uint32_t ph = n & 1;
         const bool more = n + 1 < n_tiles;
         const uint32_t q_a = ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE);
-        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + buf * L::TILE);
+        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? buf : 0) * L::TILE);
         // dV += P^T dO (B = dO as [queries][D], N contiguous)
         if (!wait_bar(p_full, ph, ctl, 53)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint64_t don = ptx::smem_desc(do_a, L::TILE, 8 * L::ROWB, L::SWZ);
+        const uint64_t don = ptx::smem_desc(do_a, L::BOX, 8 * L::BOXB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDV, tmem + kColS + kb * 8 + (kb >= 4 ? 32 : 0), don + ((kb * 16 * L::ROWB) >> 4),
+          ptx::mma_ts(tmem + kColDV, tmem + kColS + kb * 8 + (kb >= 4 ? 32 : 0), don + ((kb * 16 * L::BOXB) >> 4),
                       ID_ACC, (n > 0 || kb > 0));
-        if (more && !issue_s(n + 1)) { ok = false; break; }
+        if (L::NDO == 1) ptx::mma_commit(do_empty);
+        if (!kLateS && more && !issue_s(n + 1)) { ok = false; break; }
         // dK += dS^T Q (dS^T of queries 64-127 sits 64 columns further on)
         if (!wait_bar(ds_full, ph, ctl, 54)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint64_t qn = ptx::smem_desc(q_a, L::TILE, 8 * L::ROWB, L::SWZ);
+        if (kLateS && more && !issue_s(n + 1)) { ok = false; break; }
+        const uint64_t qn = ptx::smem_desc(q_a, L::BOX, 8 * L::BOXB, L::SWZ);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8 + (kb >= 4 ? 32 : 0), qn + ((kb * 16 * L::ROWB) >> 4),
+          ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8 + (kb >= 4 ? 32 : 0), qn + ((kb * 16 * L::BOXB) >> 4),
                       ID_ACC, (n > 0 || kb > 0));
-        if (more) issue_dp(n + 1);
+        if (!kWide && more) issue_dp(n + 1);
         // dQ = dS K once the dQ warps have read the previous one
         if (!wait_bar(dq_free, ph ^ 1u, ctl, 55)) { ok = false; break; }
         ptx::tc_fence_after();
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ss(tmem + kColDQ, dsa + ((kb * 16 * 128) >> 4), kn + ((kb * 16 * L::ROWB) >> 4), ID_DQ, kb > 0);
+          ptx::mma_ss(tmem + kColDQ, dsa + ((kb * 16 * 128) >> 4), kn + ((kb * 16 * L::BOXB) >> 4), ID_DQ, kb > 0);
         ptx::mma_commit(dq_full);
         ptx::mma_commit(&q_empty[buf]);
+        if (kWide && more) {
+          if (!wait_bar(dq_free, ph, ctl, 59)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (!issue_dp(n + 1)) { ok = false; break; }
+        }
       }
       ptx::mma_commit(done);
       wait_drain(done, 0u, drain_ns);
@@ -314,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t cS = kColS + 64 * hf;     // S^T
     const uint32_t cP = cS;                  // P^T, bf16 pairs, over the S^T just read
-    const uint32_t cSech = kColSech + 32 * hf;  // softcap: sech^2, fp16 pairs
+    const uint32_t cSech = kColSech + kSechHalf * hf;  // softcap: sech^2, fp16 pairs
     const uint32_t cDP = kColDP + 64 * hf;   // dP^T; dS^T as bf16 pairs over its first 32 columns
     int cqlo, cqhi;
     col_bounds(p, b, kg < p.Lk ? kg : p.Lk - 1, cqlo, cqhi);
@@ -328,7 +392,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float ikc = SCORE == SCORE_SOFTCAP ? 1.0f / kcap : 0.f;
     const float2 ikc2 = make_float2(ikc, ikc);
     bool ok = true;
-    if (kKVT && n_tiles > 0) {
+    if constexpr (kKVT) if (n_tiles > 0) {
       // this thread's key row of K (half 0) or V (half 1) into TMEM: 16-byte
       // chunk c of row r sits at c ^ (r & 7) (128-byte rows) or
       // c ^ ((r >> 1) & 3) (64-byte rows) of the swizzled tile
@@ -530,22 +594,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && __all_sync(0xffffffffu, wait_bar(done, 0u, ctl, 63))) {
       ptx::tc_fence_after();
       const int64_t roff = ((static_cast<int64_t>(b) * p.Hkv + hkv) * p.Lk + kg) * D;
-      float a[D];
-#pragma unroll
-      for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + (hf ? kColDK : kColDV) + c, &a[c]);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
       const float f = (hf && n_tiles > 0) ? p.scale : 1.0f;
+      const bool z = n_tiles == 0;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hf ? p.dk : p.dv) + roff);
-      if (kg < p.Lk) {
-        const bool z = n_tiles == 0;
+      constexpr int EC = D < 64 ? D : 64;  // columns per TMEM read-out
 #pragma unroll
-        for (int c = 0; c < D; c += 8)
-          dst[c / 8] = make_uint4(ptx::pack_bf16x2(z ? 0.f : a[c] * f, z ? 0.f : a[c + 1] * f),
-                                  ptx::pack_bf16x2(z ? 0.f : a[c + 2] * f, z ? 0.f : a[c + 3] * f),
-                                  ptx::pack_bf16x2(z ? 0.f : a[c + 4] * f, z ? 0.f : a[c + 5] * f),
-                                  ptx::pack_bf16x2(z ? 0.f : a[c + 6] * f, z ? 0.f : a[c + 7] * f));
+      for (int c0 = 0; c0 < D; c0 += EC) {
+        float a[EC];
+#pragma unroll
+        for (int c = 0; c < EC; c += 32) ptx::tmem_ld32f(tl + (hf ? kColDK : kColDV) + c0 + c, &a[c]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < EC; c += 32) ptx::reg_fence32f(&a[c]);
+        if (kg < p.Lk) {
+#pragma unroll
+          for (int c = 0; c < EC; c += 8)
+            dst[(c0 + c) / 8] = make_uint4(ptx::pack_bf16x2(z ? 0.f : a[c] * f, z ? 0.f : a[c + 1] * f),
+                                           ptx::pack_bf16x2(z ? 0.f : a[c + 2] * f, z ? 0.f : a[c + 3] * f),
+                                           ptx::pack_bf16x2(z ? 0.f : a[c + 4] * f, z ? 0.f : a[c + 5] * f),
+                                           ptx::pack_bf16x2(z ? 0.f : a[c + 6] * f, z ? 0.f : a[c + 7] * f));
+        }
       }
     }
     ptx::tc_fence_before();
@@ -570,29 +638,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool got = __all_sync(0xffffffffu, wait_bar(dq_full, n & 1u, ctl, 70));
       if (!ptx::named_bar_and(kBarDQ, kDQThreads, got)) { ok = false; break; }
       ptx::tc_fence_after();
-      float a[D];
-#pragma unroll
-      for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + kColDQ + c, &a[c]);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(dq_free);
-      // the previous tile's reduction has read the staging buffer
-      if (issuer) ptx::bulk_wait_group_read0();
-      ptx::named_bar_sync(kBarDQ, kDQThreads);
       uint8_t* sb = smem + L::OFF_DQS;
+      // the reduction that last read the staging buffer is done with it
+      auto staging_free = [&]() {
+        if (issuer) ptx::bulk_wait_group_read0();
+        ptx::named_bar_sync(kBarDQ, kDQThreads);
+      };
+      // row r's 32 fp32 values into staging box sbx
+      auto store_box = [&](const float* a, int sbx) {
+        uint8_t* box = sb + sbx * (128 * 128);
 #pragma unroll
-      for (int c = 0; c < D; c += 4)
-        *reinterpret_cast<float4*>(sb + (c >> 5) * (128 * 128) + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4)) =
-            make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(kBarDQ, kDQThreads);
-      if (issuer) {
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(box + r * 128 + (((c >> 2) ^ (r & 7)) << 4)) =
+              make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
+      };
+      // staging boxes [0, nbx) -> channels 32 (bx0 + i) of the accumulator
+      auto reduce_staged = [&](int bx0, int nbx) {
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kBarDQ, kDQThreads);
+        if (issuer) {
+          for (int i = 0; i < nbx; ++i)
+            ptx::tma_reduce_add_3d(&tmDQ, sb + i * (128 * 128), 32 * (bx0 + i), i0, b * p.Hq + h);
+          ptx::bulk_commit_group();
+        }
+      };
+      if constexpr (D <= 64) {
+        float a[D];
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) ptx::tma_reduce_add_3d(&tmDQ, sb + bx * (128 * 128), 32 * bx, i0, b * p.Hq + h);
-        ptx::bulk_commit_group();
+        for (int c = 0; c < D; c += 32) ptx::tmem_ld32f(tl + kColDQ + c, &a[c]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < D; c += 32) ptx::reg_fence32f(&a[c]);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(dq_free);
+        staging_free();
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) store_box(&a[32 * bx], bx);
+        reduce_staged(0, D / 32);
+      } else {
+        // d = 128 through one staging box: channels 0-31 go out first, 32-127
+        // wait in registers; dQ's TMEM (shared with dP^T) is released once
+        // all are read
+        float a0[32], a1[96];
+        ptx::tmem_ld32f(tl + kColDQ, &a0[0]);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32f(&a0[0]);
+        staging_free();
+        store_box(a0, 0);
+        reduce_staged(0, 1);
+#pragma unroll
+        for (int c = 0; c < 96; c += 32) ptx::tmem_ld32f(tl + kColDQ + 32 + c, &a1[c]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 96; c += 32) ptx::reg_fence32f(&a1[c]);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(dq_free);
+#pragma unroll
+        for (int bx = 1; bx < 4; ++bx) {
+          staging_free();
+          store_box(&a1[32 * (bx - 1)], 0);
+          reduce_staged(bx, 1);
+        }
       }
     }
     if (issuer) ptx::bulk_wait_group0();
@@ -683,7 +791,11 @@ cudaError_t launch_bwd_d(int score_mod, const CUtensorMap* maps, const BwdParams
 }  // namespace
 
 cudaError_t launch_bwd(int d, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
-  return d == 32 ? launch_bwd_d<32>(score_mod, maps, p, s) : launch_bwd_d<64>(score_mod, maps, p, s);
+  switch (d) {
+    case 32: return launch_bwd_d<32>(score_mod, maps, p, s);
+    case 64: return launch_bwd_d<64>(score_mod, maps, p, s);
+    default: return launch_bwd_d<128>(score_mod, maps, p, s);
+  }
 }
 
 }  // namespace fl

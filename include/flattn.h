@@ -241,7 +241,7 @@ FL_API size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc);
  *   workspace        : caller-owned device buffer of at least
  *                      fl_attn_bwd_workspace_size(desc) bytes (16-byte
  *                      aligned): an fp32 dq accumulator and two per-row vectors
- * desc: the forward's descriptor; d == dv in {32, 64}, Lq a multiple of 4,
+ * desc: the forward's descriptor; d == dv in {32, 64, 128}, Lq a multiple of 4,
  * strides zero.  Masks, ALiBi and softcap as in fl_attn_fwd.
  */
 FL_API fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,

@@ -154,6 +154,37 @@ def test_decode_rejects(L):
     assert f(P, P, P, P, 0, 0, 0, z, ctypes.byref(dd(score_mod=1))) == _lib.FL_ERR_INVALID_ARG
 
 
+def test_bwd_rejects(L):
+    """fl_attn_bwd's argument checks, all of which return before any CUDA
+    call; d = dv = 128 passes the dimension check and is stopped here only by
+    the workspace size."""
+    f = L.fl_attn_bwd
+    ws = L.fl_attn_bwd_workspace_size
+
+    def call(desc, ptr=P, nbytes=None, **over):
+        args = dict(q=P, k=P, v=P, out=P, dout=P, lse=P, dq=P, dk=P, dv=P, workspace=P)
+        args.update(over)
+        n = ws(ctypes.byref(desc)) if nbytes is None else nbytes
+        return f(*args.values(), ctypes.c_size_t(n), ctypes.byref(desc))
+
+    assert f(P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t(1 << 30), None) == _lib.FL_ERR_INVALID_ARG
+    assert call(_desc(), lse=0) == _lib.FL_ERR_INVALID_ARG
+    for d, dv in ((96, 96), (64, 128), (128, 64), (256, 256), (16, 16)):
+        assert call(_desc(d=d, dv=dv)) == _lib.FL_ERR_UNSUPPORTED, (d, dv)
+    assert call(_desc(mask_kind=1, Lk=256)) == _lib.FL_ERR_UNSUPPORTED      # masked Lq != Lk
+    assert call(_desc(Lq=130, Lk=130)) == _lib.FL_ERR_UNSUPPORTED           # Lq % 4
+    assert call(_desc(score_mod=2, softcap=0.0)) == _lib.FL_ERR_INVALID_ARG
+    assert call(_desc(score_mod=1)) == _lib.FL_ERR_INVALID_ARG              # ALiBi without slopes
+    assert call(_desc(), dk=P + 8) == _lib.FL_ERR_ALIGNMENT
+    assert call(_desc(), lse=P + 2) == _lib.FL_ERR_ALIGNMENT
+    for d in (32, 64, 128):
+        desc = _desc(d=d, dv=d)
+        need = ws(ctypes.byref(desc))
+        assert need == 1 * 2 * 128 * (d + 2) * 4
+        assert call(desc, nbytes=need - 1) == _lib.FL_ERR_INVALID_ARG, d
+        assert call(desc, workspace=0) == _lib.FL_ERR_INVALID_ARG, d
+
+
 def test_decode_split_arithmetic():
     """Host split rule (mirrors csrc/decode.h): enough CTAs for four per SM
     (up to 8 query rows per CTA) or sixteen per SM (more rows), every split a

@@ -45,6 +45,16 @@ CASES = [
     (1, 2, 2, 300, 32, None, dict(mask="causal")),
     (1, 4, 2, 1000, 32, None, dict(score_mod="softcap", softcap=20.0, mask="causal")),
     (2, 4, 4, 1024, 64, None, dict(mask="causal")),
+    # d = 128: its own TMEM map (dQ sharing dP^T's columns), one dO buffer
+    (1, 2, 2, 256, 128, None, dict()),
+    (1, 2, 2, 300, 128, None, dict(mask="causal")),
+    (1, 4, 2, 520, 128, None, dict(mask="window", window=100)),
+    (1, 2, 2, 400, 128, None, dict(mask="prefix_lm", prefix=150)),
+    (2, 2, 2, 500, 128, 4, dict(mask="document", doc_causal=True)),
+    (1, 4, 4, 300, 128, None, dict(score_mod="alibi", mask="causal")),
+    (1, 2, 2, 300, 128, None, dict(score_mod="softcap", softcap=5.0)),
+    (1, 4, 2, 1000, 128, None, dict(score_mod="softcap", softcap=20.0, mask="causal")),
+    (2, 8, 2, 1024, 128, None, dict(mask="causal")),
 ]
 
 
@@ -110,6 +120,26 @@ def test_bwd_fullsize_sampled_heads(kw):
     for b, h in ((0, 0), (1, 7), (3, 15)):
         sl = (slice(b, b + 1), slice(h, h + 1))
         rq, rk, rv = oracle.attention_backward(q[sl], k[sl], v[sl], dout[sl], **okw)
+        _cmp(dq[sl], rq, f"dq[{b},{h}]")
+        _cmp(dk[sl], rk, f"dk[{b},{h}]")
+        _cmp(dv[sl], rv, f"dv[{b},{h}]")
+
+
+# The d = 128 forward's workload (causal, B 2, H 16, L 4096): dq, dk, dv of
+# three sampled heads against the oracle's exact gradients of those heads.
+@pytest.mark.parametrize("kw", [dict(mask="causal"), dict(score_mod="softcap", softcap=30.0)],
+                         ids=["causal", "softcap30"])
+def test_bwd_d128_fullsize_sampled_heads(kw):
+    B, H, L, d = 2, 16, 4096, 128
+    q, k, v = synth.attn_inputs(B, H, H, L, d, seed=92)
+    dout = synth.randn_bf16((B, H, L, d), synth.generator(93))
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    out, lse = attn_fwd(qd, kd, vd, **kw)
+    dq, dk, dv = attn_bwd(qd, kd, vd, out, dod, lse, **kw)
+    sync_status()
+    for b, h in ((0, 0), (1, 9), (1, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        rq, rk, rv = oracle.attention_backward(q[sl], k[sl], v[sl], dout[sl], **kw)
         _cmp(dq[sl], rq, f"dq[{b},{h}]")
         _cmp(dk[sl], rk, f"dk[{b},{h}]")
         _cmp(dv[sl], rv, f"dv[{b},{h}]")
