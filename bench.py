@@ -161,7 +161,7 @@ def make_calls(api, bufs, slopes):
 # another family uses, so a change to (say) the backward leaves the forward
 # kernels' counters valid.
 KERNEL_FAMILY_EXCLUDES = {"forward": ("bwd.", "decode."), "backward": ("decode.",), "decode": ("bwd.",)}
-TRAFFIC_FAMILY = {"decode": "decode", "backward": "backward"}  # every other entry: forward
+TRAFFIC_FAMILY = {"decode": "decode", "backward": "backward", "backward_d128": "backward"}  # else forward
 
 
 def kernel_source_hash(family="forward"):
@@ -282,7 +282,8 @@ def variant_configs():
 
             def call():
                 api.attn_bwd(q, k, v, out, dout, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
-            return call, tf, ef, by, "1 input set (100 MB of inputs and outputs; dq accumulator 67 MB)"
+            mb = (8 * q.numel() * 2 + q.numel() * 4) / 1e6
+            return call, tf, ef, by, f"1 input set ({mb:.0f} MB of inputs, outputs and dq accumulator)"
         return name, build
 
     def evo():
@@ -314,6 +315,7 @@ def variant_configs():
         decode(),
         bwd("7 backward B4 H16 L2048 d64 causal", 4, 16, 2048, 64, 90, mask="causal"),
         attn("8 d128 causal B2 H16 L4096 d128", 2, 16, 16, 4096, 128, 2, 70, mask="causal"),
+        bwd("9 backward d128 B2 H16 L4096 causal", 2, 16, 4096, 128, 92, mask="causal"),
     ]
 
 
