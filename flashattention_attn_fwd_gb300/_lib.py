@@ -41,6 +41,8 @@ EXPORTS = (
     "fl_attn_decode_workspace_size",
     "fl_attn_bwd",
     "fl_attn_bwd_workspace_size",
+    "fl_diffattn_bwd",
+    "fl_diffattn_bwd_workspace_size",
     "fl_last_error_detail",
     "fl_attn_schedule",
 )
@@ -107,6 +109,11 @@ def lib() -> ctypes.CDLL:
         L.fl_attn_bwd.restype = i32
         L.fl_attn_bwd_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
         L.fl_attn_bwd_workspace_size.restype = ctypes.c_size_t
+        L.fl_diffattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_size_t, ctypes.POINTER(AttnDesc)]
+        L.fl_diffattn_bwd.restype = i32
+        L.fl_diffattn_bwd_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
+        L.fl_diffattn_bwd_workspace_size.restype = ctypes.c_size_t
         L.fl_sync_status.argtypes = [vp]
         L.fl_sync_status.restype = i32
         L.fl_attn_schedule.argtypes = [ctypes.POINTER(AttnDesc), vp, ctypes.POINTER(ctypes.c_int64)]

@@ -131,6 +131,37 @@ def diffattn_fwd(q1, k1, q2, k2, v, lam: float, *, causal: bool = True, scale: f
     return out, lse
 
 
+def diffattn_bwd(q1, k1, q2, k2, v, dout, lam: float, *, causal: bool = True, scale: float | None = None,
+                 dq1=None, dk1=None, dq2=None, dk2=None, dv=None, workspace=None, stream=None):
+    """fl_diffattn_bwd: gradients (dq1, dk1, dq2, dk2, dv) of diffattn_fwd's
+    out for the output gradient dout [B,H,L,128]; contiguous bf16 tensors."""
+    for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v), ("dout", dout)):
+        _need(t, name, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, H, L, d = q1.shape
+    dq1 = torch.empty_like(q1) if dq1 is None else dq1
+    dk1 = torch.empty_like(k1) if dk1 is None else dk1
+    dq2 = torch.empty_like(q2) if dq2 is None else dq2
+    dk2 = torch.empty_like(k2) if dk2 is None else dk2
+    dv = torch.empty_like(v) if dv is None else dv
+    desc = _lib.new_desc()
+    desc.B, desc.Hq, desc.Hkv, desc.Lq, desc.Lk, desc.d, desc.dv = B, H, H, L, L, d, v.shape[-1]
+    desc.scale = 0.0 if scale is None else float(scale)
+    desc.mask_kind = MASKS["causal" if causal else "none"]
+    desc.stream = _stream_ptr(stream)
+    need = int(_lib.lib().fl_diffattn_bwd_workspace_size(ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q1.device, dtype=torch.uint8)
+    st = _lib.lib().fl_diffattn_bwd(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(), v.data_ptr(),
+                                    dout.data_ptr(), ctypes.c_float(float(lam)), dq1.data_ptr(), dk1.data_ptr(),
+                                    dq2.data_ptr(), dk2.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                                    ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                    ctypes.byref(desc))
+    _lib.check(st, "fl_diffattn_bwd")
+    return dq1, dk1, dq2, dk2, dv
+
+
 def evoformer_gated_attn_fwd(q, k, v, pair_bias, mask_bias, gate, *, scale: float | None = None,
                              out=None, lse=None, return_lse: bool = True, stream=None):
     """fl_evoformer_gated_attn_fwd: q,k,v,gate [B,N_seq,H,N_res,d] bf16,

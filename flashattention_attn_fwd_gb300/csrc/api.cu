@@ -463,13 +463,18 @@ size_t fl_attn_bwd_workspace_size(const fl_attn_desc* desc) {
   return rows * (static_cast<size_t>(desc->d) + 2) * sizeof(float);
 }
 
-fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
-                      const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                      const fl_attn_desc* desc) {
+namespace {
+
+// fl_attn_bwd for the gradients of dout_scale * dout, adding dV to dv's
+// contents when dv_accumulate (the differential backward's second branch).
+fl_status attn_bwd_run(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       const fl_attn_desc* desc, float dout_scale, bool dv_accumulate) {
   if (!desc || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FL_ERR_INVALID_ARG;
   const fl_attn_desc& d = *desc;
   if (d.B < 1 || d.Hq < 1 || d.Hkv < 1 || d.Lq < 1 || d.Lk < 1 || d.Hq % d.Hkv != 0) return FL_ERR_INVALID_ARG;
-  if (d.d != d.dv || (d.d != 32 && d.d != 64 && d.d != 128)) return FL_ERR_UNSUPPORTED;
+  const bool same = d.d == d.dv && (d.d == 32 || d.d == 64 || d.d == 128);
+  if (!same && !(d.d == 64 && d.dv == 128)) return FL_ERR_UNSUPPORTED;
   if (!std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
   if (d.mask_kind < FL_MASK_NONE || d.mask_kind > FL_MASK_DOCUMENT) return FL_ERR_INVALID_ARG;
   if (d.mask_kind != FL_MASK_NONE && d.Lq != d.Lk) return FL_ERR_UNSUPPORTED;
@@ -507,12 +512,14 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.d));
   p.softcap = d.softcap;
   if (d.score_mod == FL_SCORE_SOFTCAP) softcap_coefficients(p, p.scale, d.softcap);
+  p.dout_scale = dout_scale;
+  p.dv_accumulate = dv_accumulate ? 1 : 0;
   p.mask_kind = d.mask_kind; p.doc_causal = d.doc_causal ? 1 : 0;
   p.window = d.window; p.prefix = d.prefix_len; p.num_docs = d.num_docs;
   if (static_cast<int64_t>(d.B) * d.Hkv * p.n_ktiles > 0x7fffffff) return FL_ERR_UNSUPPORTED;
   CUtensorMap maps[7];
-  const int bw = box_width(d.d);
-  const int64_t sl = d.d;
+  const int bw = box_width(d.d), bwv = box_width(d.dv);
+  const int64_t sl = d.d, slv = d.dv;
   // the fp32 dQ accumulator as [B * Hq][Lq][d], boxes of 32 channels x 128
   // rows (the target of the kernel's bulk reductions)
   const uint64_t qa_dims[3] = {static_cast<uint64_t>(d.d), static_cast<uint64_t>(d.Lq),
@@ -523,16 +530,72 @@ fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* o
                    static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
       !encode_bhlc(&maps[1], k, d.d, d.Lk, d.Hkv, d.B, sl, static_cast<int64_t>(d.Lk) * d.d,
                    static_cast<int64_t>(d.Hkv) * d.Lk * d.d, bw) ||
-      !encode_bhlc(&maps[2], v, d.d, d.Lk, d.Hkv, d.B, sl, static_cast<int64_t>(d.Lk) * d.d,
-                   static_cast<int64_t>(d.Hkv) * d.Lk * d.d, bw) ||
-      !encode_bhlc(&maps[3], dout, d.d, d.Lq, d.Hq, d.B, sl, static_cast<int64_t>(d.Lq) * d.d,
-                   static_cast<int64_t>(d.Hq) * d.Lq * d.d, bw) ||
+      !encode_bhlc(&maps[2], v, d.dv, d.Lk, d.Hkv, d.B, slv, static_cast<int64_t>(d.Lk) * d.dv,
+                   static_cast<int64_t>(d.Hkv) * d.Lk * d.dv, bwv) ||
+      !encode_bhlc(&maps[3], dout, d.dv, d.Lq, d.Hq, d.B, slv, static_cast<int64_t>(d.Lq) * d.dv,
+                   static_cast<int64_t>(d.Hq) * d.Lq * d.dv, bwv) ||
       !encode_rows_f32(&maps[4], p.l2, static_cast<int64_t>(d.B) * d.Hq, d.Lq) ||
       !encode_rows_f32(&maps[5], p.dvec, static_cast<int64_t>(d.B) * d.Hq, d.Lq) ||
       !encode(&maps[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.dq_acc, qa_dims, qa_str, qa_box,
               CU_TENSOR_MAP_SWIZZLE_128B))
     return cuda_fail("cuTensorMapEncodeTiled", cudaSuccess);
-  return launched("backward kernel launch", fl::launch_bwd(d.d, d.score_mod, maps, p, static_cast<cudaStream_t>(d.stream)));
+  return launched("backward kernel launch", fl::launch_bwd(d.d, d.dv, d.score_mod, maps, p, static_cast<cudaStream_t>(d.stream)));
+}
+
+}  // namespace
+
+fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      const fl_attn_desc* desc) {
+  return attn_bwd_run(q, k, v, out, dout, lse, dq, dk, dv, workspace, workspace_bytes, desc, 1.0f, false);
+}
+
+size_t fl_diffattn_bwd_workspace_size(const fl_attn_desc* desc) {
+  if (!desc || desc->B < 1 || desc->Hq < 1 || desc->Lq < 1) return 0;
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Hq * desc->Lq;
+  // O1, O2 (bf16, dv = 128), the backward's workspace (d = 64), LSE1, LSE2
+  return rows * (2 * 128 * 2 + (64 + 2) * 4 + 2 * 4);
+}
+
+fl_status fl_diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                          const void* dout, float lambda, void* dq1, void* dk1, void* dq2, void* dk2, void* dv,
+                          void* workspace, size_t workspace_bytes, const fl_attn_desc* desc) {
+  if (!desc || !q1 || !k1 || !q2 || !k2 || !v || !dout || !dq1 || !dk1 || !dq2 || !dk2 || !dv)
+    return FL_ERR_INVALID_ARG;
+  const fl_attn_desc& d = *desc;
+  if (d.B < 1 || d.Hq < 1 || d.Lq < 1 || d.Hkv != d.Hq || d.Lk != d.Lq) return FL_ERR_INVALID_ARG;
+  if (!std::isfinite(lambda) || !std::isfinite(d.scale)) return FL_ERR_INVALID_ARG;
+  if (d.d != 64 || d.dv != 128) return FL_ERR_UNSUPPORTED;
+  if (d.mask_kind != FL_MASK_NONE && d.mask_kind != FL_MASK_CAUSAL) return FL_ERR_UNSUPPORTED;
+  if (d.score_mod != FL_SCORE_NONE) return FL_ERR_UNSUPPORTED;
+  for (int i = 0; i < 4; ++i)
+    if (d.q_strides[i] || d.k_strides[i] || d.v_strides[i] || d.o_strides[i]) return FL_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q1, k1, q2, k2, v, dout, dq1, dk1, dq2, dk2, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FL_ERR_ALIGNMENT;
+  if (d.Lq % 4 != 0) return FL_ERR_UNSUPPORTED;  // as fl_attn_bwd
+  const size_t need = fl_diffattn_bwd_workspace_size(desc);
+  if (!workspace || workspace_bytes < need) return FL_ERR_INVALID_ARG;
+
+  // each branch is softmax attention (d 64, dv 128) over the shared V; the
+  // fused forward keeps only O1 - lambda O2, so O1, O2 and their LSEs are
+  // recomputed into the workspace: [O1 | O2 | backward workspace | LSE1 | LSE2]
+  fl_attn_desc a = d;
+  a.scale = d.scale > 0.f ? d.scale : 0.125f;
+  const size_t rows = static_cast<size_t>(d.B) * d.Hq * d.Lq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* o1 = ws;
+  void* o2 = ws + rows * 256;
+  void* bws = ws + rows * 512;
+  const size_t bws_bytes = rows * (64 + 2) * 4;
+  float* lse1 = reinterpret_cast<float*>(ws + rows * 512 + bws_bytes);
+  float* lse2 = lse1 + rows;
+  fl_status st = fl_attn_fwd(q1, k1, v, o1, lse1, &a);
+  if (st == FL_OK) st = fl_attn_fwd(q2, k2, v, o2, lse2, &a);
+  // d/dO1 = dout, d/dO2 = -lambda dout; dV sums both branches
+  if (st == FL_OK) st = attn_bwd_run(q1, k1, v, o1, dout, lse1, dq1, dk1, dv, bws, bws_bytes, &a, 1.0f, false);
+  if (st == FL_OK) st = attn_bwd_run(q2, k2, v, o2, dout, lse2, dq2, dk2, dv, bws, bws_bytes, &a, -lambda, true);
+  return st;
 }
 
 size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc) {

@@ -67,24 +67,32 @@ constexpr int kBwdLaunchRegs = 128, kBwdCtlRegs = 56, kBwdComputeRegs = 168, kBw
 static_assert(128 * kBwdCtlRegs + 256 * kBwdComputeRegs + 128 * kBwdDQRegs <= kBwdThreads * kBwdLaunchRegs,
               "backward register split");
 
-template <int D>
+template <int D, int DV>
 struct BwdLayout {
-  static_assert(D == 32 || D == 64 || D == 128, "backward head dim");
+  static_assert((D == DV && (D == 32 || D == 64 || D == 128)) || (D == 64 && DV == 128), "backward head dims");
   static constexpr int ROWB = D * 2;
-  static constexpr int BOXW = D < 64 ? D : 64;         // channels per TMA box (rows of <= 128 bytes)
+  // Q and K: D channels; V and dO: DV channels; each in boxes of at most 64
+  // channels (128-byte rows)
+  static constexpr int BOXW = D < 64 ? D : 64;
   static constexpr int NBOX = D / BOXW;
   static constexpr int BOXB = BOXW * 2;                // bytes per row of one box
   static constexpr int BOX = 128 * BOXB;               // one box of 128 rows
-  static constexpr int TILE = NBOX * BOX;              // one 128-row tile of K, V, Q or dO
+  static constexpr int TILE = NBOX * BOX;              // one 128-row tile of K or Q
   static constexpr uint32_t SWZ = BOXB == 128 ? 2u : 4u;
+  static constexpr int BOXW_V = DV < 64 ? DV : 64;
+  static constexpr int NBOX_V = DV / BOXW_V;
+  static constexpr int BOXB_V = BOXW_V * 2;
+  static constexpr int BOX_V = 128 * BOXB_V;
+  static constexpr int TILE_V = NBOX_V * BOX_V;        // one 128-row tile of V or dO
+  static constexpr uint32_t SWZ_V = BOXB_V == 128 ? 2u : 4u;
   // d = 128: one dO buffer and one 32-channel dQ staging box; two of each
   // would not fit in a block's 227 KB
   static constexpr int NDO = D == 128 ? 1 : 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
-  static constexpr int OFF_Q = 2 * TILE;               // Q[2]
-  static constexpr int OFF_DO = 4 * TILE;              // dO[NDO]
-  static constexpr int OFF_DS = OFF_DO + NDO * TILE;   // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
+  static constexpr int OFF_Q = TILE + TILE_V;          // Q[2]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;      // dO[NDO]
+  static constexpr int OFF_DS = OFF_DO + NDO * TILE_V; // dS tile: 2 boxes [128 keys][64 queries], 128B swizzle
   static constexpr int DQS = D == 128 ? 128 * 32 * 4 : 128 * D * 4;  // fp32 boxes [128 rows][32], 128B swizzle
   static constexpr int OFF_DQS = OFF_DS + 2 * 128 * 128;  // dQ staging (the previous tile's reduction
                                                           // has a whole tile period to read it out)
@@ -94,9 +102,17 @@ struct BwdLayout {
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static_assert(SMEM <= 227 * 1024, "backward shared memory");
-  // k-step kb (16 channels) of a K-major tile: box kb * 16 / BOXW, 32 bytes
-  // per step within the box's 128-byte swizzled rows (descriptor units of 16 B)
-  __host__ __device__ static constexpr uint32_t koff(int kb) { return ((kb * 16 / BOXW) * BOX + (kb * 16 % BOXW) * 2) >> 4; }
+  static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_DQS % 1024 == 0,
+                "swizzled tiles on 1024-byte boundaries");
+  // k-step kb (16 channels) of a K-major Q / K tile: box kb * 16 / BOXW, 32
+  // bytes per step within the box's 128-byte swizzled rows (descriptor
+  // units of 16 B); koff_v likewise for V / dO
+  __host__ __device__ static constexpr uint32_t koff(int kb) {
+    return ((kb * 16 / BOXW) * BOX + (kb * 16 % BOXW) * 2) >> 4;
+  }
+  __host__ __device__ static constexpr uint32_t koff_v(int kb) {
+    return ((kb * 16 / BOXW_V) * BOX_V + (kb * 16 % BOXW_V) * 2) >> 4;
+  }
 };
 
 // Queries that see key k form one interval [qlo, qhi] for every mask kind
@@ -125,27 +141,31 @@ __device__ __forceinline__ void col_bounds(const BwdParams& p, int b, int k, int
   qhi = qhi > p.Lq - 1 ? p.Lq - 1 : qhi;
 }
 
-template <int D, int SCORE>
+template <int D, int DV, int SCORE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmDv,
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
-  using L = BwdLayout<D>;
-  // d <= 64: S^T [0,128), K V or sech^2 [128,192), dP^T [192,320), dV, dK, dQ
-  // after.  d = 128 (dV and dK take 256 columns): S^T [0,128), dP^T [128,256)
-  // shared with dQ, dV [256,384), dK [384,512); softcap's sech^2 goes over the
-  // second half of each half-tile's S^T columns (P^T holds the first).
+  using L = BwdLayout<D, DV>;
+  // d = dv <= 64: S^T [0,128), K V or sech^2 [128,192), dP^T [192,320), dV,
+  // dK, dQ after.  d = 128 (dV and dK take 256 columns): S^T [0,128), dP^T
+  // [128,256) shared with dQ, dV [256,384), dK [384,512).  d = 64 with dv =
+  // 128: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,448), dQ
+  // [448,512).  In the last two maps softcap's sech^2 goes over the second
+  // half of each half-tile's S^T columns (P^T holds the first).
   constexpr bool kWide = D == 128;
-  constexpr uint32_t kColS = 0, kColDP = kWide ? 128 : 192, kColDV = kWide ? 256 : 320;
-  constexpr uint32_t kColDK = kColDV + D, kColDQ = kWide ? kColDP : 320 + 2 * D;
-  // TMEM [128,192) (d <= 64): K and V without softcap, the tile's sech^2 with it
-  constexpr bool kKVT = SCORE != SCORE_SOFTCAP && !kWide;
+  constexpr bool kSechInS = D == 128 || DV != D;
+  constexpr uint32_t kColS = 0, kColDP = kSechInS ? 128 : 192, kColDV = kSechInS ? 256 : 320;
+  constexpr uint32_t kColDK = kColDV + DV, kColDQ = kWide ? kColDP : kColDK + D;
+  static_assert(kColDK + D <= 512 && kColDQ + D <= 512, "backward TMEM map");
+  // TMEM [128,192) (d = dv <= 64): K and V without softcap, the tile's sech^2 with it
+  constexpr bool kKVT = SCORE != SCORE_SOFTCAP && !kSechInS;
   constexpr uint32_t kColKT = 128, kColVT = 128 + D / 2;
   // softcap: sech^2, fp16 pairs, 32 columns per half
-  constexpr uint32_t kColSech = kWide ? 32 : 128, kSechHalf = kWide ? 64 : 32;
-  // d = 128 softcap: the next S^T overwrites sech^2, so it waits for the dS step
-  constexpr bool kLateS = kWide && SCORE == SCORE_SOFTCAP;
+  constexpr uint32_t kColSech = kSechInS ? 32 : 128, kSechHalf = kSechInS ? 64 : 32;
+  // sech^2 in the S^T columns: the next S^T waits for the dS step
+  constexpr bool kLateS = kSechInS && SCORE == SCORE_SOFTCAP;
   extern __shared__ uint8_t bsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -220,12 +240,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---------------------------------------------------------------- TMA
       const uint64_t pol_keep = ptx::policy_evict_last();
       if (n_tiles > 0) {
-        ptx::mbar_arrive_expect_tx(kv_full, 2u * L::TILE);
+        ptx::mbar_arrive_expect_tx(kv_full, static_cast<uint32_t>(L::TILE + L::TILE_V));
 #pragma unroll
-        for (int bx = 0; bx < L::NBOX; ++bx) {
+        for (int bx = 0; bx < L::NBOX; ++bx)
           ptx::tma_load_4d(smem + L::OFF_K + bx * L::BOX, &tmK, kv_full, bx * L::BOXW, j0, hkv, b, pol_keep);
-          ptx::tma_load_4d(smem + L::OFF_V + bx * L::BOX, &tmV, kv_full, bx * L::BOXW, j0, hkv, b, pol_keep);
-        }
+#pragma unroll
+        for (int bx = 0; bx < L::NBOX_V; ++bx)
+          ptx::tma_load_4d(smem + L::OFF_V + bx * L::BOX_V, &tmV, kv_full, bx * L::BOXW_V, j0, hkv, b, pol_keep);
       }
       int issued = 0, do_issued = 0;
       bool ok = true;
@@ -233,14 +254,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = hkv * group + n / nq, i0 = (it_lo + n % nq) * 128;
         const int buf = n & 1;
         if (!wait_bar(&q_empty[buf], ((n >> 1) & 1u) ^ 1u, ctl, 50)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(&q_full[buf], (L::NDO == 2 ? 2u : 1u) * L::TILE + 2u * 512u);
+        ptx::mbar_arrive_expect_tx(&q_full[buf],
+                                   static_cast<uint32_t>(L::TILE + (L::NDO == 2 ? L::TILE_V : 0)) + 2u * 512u);
 #pragma unroll
-        for (int bx = 0; bx < L::NBOX; ++bx) {
+        for (int bx = 0; bx < L::NBOX; ++bx)
           ptx::tma_load_4d(smem + L::OFF_Q + buf * L::TILE + bx * L::BOX, &tmQ, &q_full[buf], bx * L::BOXW, i0, h, b,
                            pol_keep);
-          if (L::NDO == 2)
-            ptx::tma_load_4d(smem + L::OFF_DO + buf * L::TILE + bx * L::BOX, &tmDO, &q_full[buf], bx * L::BOXW, i0,
-                             h, b, pol_keep);
+        if (L::NDO == 2) {
+#pragma unroll
+          for (int bx = 0; bx < L::NBOX_V; ++bx)
+            ptx::tma_load_4d(smem + L::OFF_DO + buf * L::TILE_V + bx * L::BOX_V, &tmDO, &q_full[buf], bx * L::BOXW_V,
+                             i0, h, b, pol_keep);
         }
         const int row = b * p.Hq + h;
         ptx::tma_load_2d(vec + buf * 128, &tmL2, &q_full[buf], i0, row, pol_keep);
@@ -249,10 +273,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (L::NDO == 1) {
           // one dO buffer: tile n's once dV(n - 1) has read tile n - 1's
           if (!wait_bar(do_empty, (n & 1u) ^ 1u, ctl, 56)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(do_full, L::TILE);
+          ptx::mbar_arrive_expect_tx(do_full, L::TILE_V);
 #pragma unroll
-          for (int bx = 0; bx < L::NBOX; ++bx)
-            ptx::tma_load_4d(smem + L::OFF_DO + bx * L::BOX, &tmDO, do_full, bx * L::BOXW, i0, h, b, pol_keep);
+          for (int bx = 0; bx < L::NBOX_V; ++bx)
+            ptx::tma_load_4d(smem + L::OFF_DO + bx * L::BOX_V, &tmDO, do_full, bx * L::BOXW_V, i0, h, b, pol_keep);
           do_issued = n + 1;
         }
       }
@@ -264,7 +288,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA
       constexpr uint32_t ID_SS = ptx::idesc_bf16_f32(128, 128, false);        // S^T, dP^T
-      constexpr uint32_t ID_ACC = ptx::idesc_bf16_f32(128, D, true);          // dV, dK (B = dO / Q, N-major)
+      constexpr uint32_t ID_DV = ptx::idesc_bf16_f32(128, DV, true);         // dV (B = dO, N-major)
+      constexpr uint32_t ID_DK = ptx::idesc_bf16_f32(128, D, true);          // dK (B = Q, N-major)
       constexpr uint32_t ID_DQ = ptx::idesc_bf16_f32(128, D, true) | (1u << 15);  // dQ: A = dS, M-major
       const uint32_t k_a = ptx::smem_u32(smem + L::OFF_K), v_a = ptx::smem_u32(smem + L::OFF_V);
       const uint32_t ds_a = ptx::smem_u32(smem + L::OFF_DS);
@@ -273,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // stride) and K-major operands (k-steps through ::koff)
       const uint64_t kn = ptx::smem_desc(k_a, L::BOX, 8 * L::BOXB, L::SWZ);
       const uint64_t ka = ptx::smem_desc(k_a, 16, 8 * L::BOXB, L::SWZ);
-      const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::BOXB, L::SWZ);
+      const uint64_t va = ptx::smem_desc(v_a, 16, 8 * L::BOXB_V, L::SWZ_V);
       // S^T = K Q^T and dP^T = V dO^T of query tile n (K-major, k-steps of 16
       // channels), each once its Q / dO tile has landed
       auto issue_s = [&](int n) -> bool {
@@ -294,12 +319,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!wait_bar(do_full, n & 1u, ctl, 57)) return false;
           ptx::tc_fence_after();
         }
-        const uint64_t dob = ptx::smem_desc(ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? (n & 1) : 0) * L::TILE),
-                                            16, 8 * L::BOXB, L::SWZ);
+        const uint64_t dob = ptx::smem_desc(
+            ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? (n & 1) : 0) * L::TILE_V), 16, 8 * L::BOXB_V, L::SWZ_V);
 #pragma unroll
-        for (int kb = 0; kb < D / 16; ++kb) {
-          if (kKVT) ptx::mma_ts(tmem + kColDP, tmem + kColVT + kb * 8, dob + L::koff(kb), ID_SS, kb > 0);
-          else ptx::mma_ss(tmem + kColDP, va + L::koff(kb), dob + L::koff(kb), ID_SS, kb > 0);
+        for (int kb = 0; kb < DV / 16; ++kb) {
+          if (kKVT) ptx::mma_ts(tmem + kColDP, tmem + kColVT + kb * 8, dob + L::koff_v(kb), ID_SS, kb > 0);
+          else ptx::mma_ss(tmem + kColDP, va + L::koff_v(kb), dob + L::koff_v(kb), ID_SS, kb > 0);
         }
         ptx::mma_commit(dp_full);
         return true;
@@ -321,15 +346,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t ph = n & 1;
         const bool more = n + 1 < n_tiles;
         const uint32_t q_a = ptx::smem_u32(smem + L::OFF_Q + buf * L::TILE);
-        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? buf : 0) * L::TILE);
+        const uint32_t do_a = ptx::smem_u32(smem + L::OFF_DO + (L::NDO == 2 ? buf : 0) * L::TILE_V);
         // dV += P^T dO (B = dO as [queries][D], N contiguous)
         if (!wait_bar(p_full, ph, ctl, 53)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint64_t don = ptx::smem_desc(do_a, L::BOX, 8 * L::BOXB, L::SWZ);
+        const uint64_t don = ptx::smem_desc(do_a, L::BOX_V, 8 * L::BOXB_V, L::SWZ_V);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
-          ptx::mma_ts(tmem + kColDV, tmem + kColS + kb * 8 + (kb >= 4 ? 32 : 0), don + ((kb * 16 * L::BOXB) >> 4),
-                      ID_ACC, (n > 0 || kb > 0));
+          ptx::mma_ts(tmem + kColDV, tmem + kColS + kb * 8 + (kb >= 4 ? 32 : 0), don + ((kb * 16 * L::BOXB_V) >> 4),
+                      ID_DV, (n > 0 || kb > 0));
         if (L::NDO == 1) ptx::mma_commit(do_empty);
         if (!kLateS && more && !issue_s(n + 1)) { ok = false; break; }
         // dK += dS^T Q (dS^T of queries 64-127 sits 64 columns further on)
@@ -340,7 +365,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb)
           ptx::mma_ts(tmem + kColDK, tmem + kColDP + kb * 8 + (kb >= 4 ? 32 : 0), qn + ((kb * 16 * L::BOXB) >> 4),
-                      ID_ACC, (n > 0 || kb > 0));
+                      ID_DK, (n > 0 || kb > 0));
         if (!kWide && more) issue_dp(n + 1);
         // dQ = dS K once the dQ warps have read the previous one
         if (!wait_bar(dq_free, ph ^ 1u, ctl, 55)) { ok = false; break; }
@@ -390,6 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float2 sq0 = make_float2(p.sc_q[0], p.sc_q[0]), sq1 = make_float2(p.sc_q[1], p.sc_q[1]);
     const float2 sq2 = make_float2(p.sc_q[2], p.sc_q[2]), sq3 = make_float2(p.sc_q[3], p.sc_q[3]);
     const float ikc = SCORE == SCORE_SOFTCAP ? 1.0f / kcap : 0.f;
+    const float gsc = p.dout_scale;  // dP of the scaled dO (D comes scaled from the pre-kernel)
     const float2 ikc2 = make_float2(ikc, ikc);
     bool ok = true;
     if constexpr (kKVT) if (n_tiles > 0) {
@@ -562,8 +588,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
-            float d0 = x[c + e4 + e] * (dpv[c + e4 + e] - dq4[e]);
-            float d1 = x[c + e4 + e + 1] * (dpv[c + e4 + e + 1] - dq4[e + 1]);
+            float d0 = x[c + e4 + e] * fmaf(dpv[c + e4 + e], gsc, -dq4[e]);
+            float d1 = x[c + e4 + e + 1] * fmaf(dpv[c + e4 + e + 1], gsc, -dq4[e + 1]);
             if (SCORE == SCORE_SOFTCAP) {
               const float2 sc = unpack_f16x2(sv[(e4 + e) >> 1]);
               d0 *= sc.x;
@@ -593,28 +619,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // is done (the TMEM loads are warp-wide; only the stores depend on the row)
     if (ok && __all_sync(0xffffffffu, wait_bar(done, 0u, ctl, 63))) {
       ptx::tc_fence_after();
-      const int64_t roff = ((static_cast<int64_t>(b) * p.Hkv + hkv) * p.Lk + kg) * D;
-      const float f = (hf && n_tiles > 0) ? p.scale : 1.0f;
       const bool z = n_tiles == 0;
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hf ? p.dk : p.dv) + roff);
-      constexpr int EC = D < 64 ? D : 64;  // columns per TMEM read-out
+      const int64_t row = (static_cast<int64_t>(b) * p.Hkv + hkv) * p.Lk + kg;
+      // NC columns of TMEM from col, times f, as bf16 into base's row (plus
+      // what is there with acc)
+      auto write_row = [&](auto nc, uint32_t col, void* base, float f, bool acc) {
+        constexpr int NC = decltype(nc)::value;
+        constexpr int EC = NC < 64 ? NC : 64;  // columns per TMEM read-out
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + row * NC);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += EC) {
-        float a[EC];
+        for (int c0 = 0; c0 < NC; c0 += EC) {
+          float a[EC];
 #pragma unroll
-        for (int c = 0; c < EC; c += 32) ptx::tmem_ld32f(tl + (hf ? kColDK : kColDV) + c0 + c, &a[c]);
-        ptx::tmem_ld_wait();
+          for (int c = 0; c < EC; c += 32) ptx::tmem_ld32f(tl + col + c0 + c, &a[c]);
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < EC; c += 32) ptx::reg_fence32f(&a[c]);
-        if (kg < p.Lk) {
+          for (int c = 0; c < EC; c += 32) ptx::reg_fence32f(&a[c]);
+          if (kg < p.Lk) {
 #pragma unroll
-          for (int c = 0; c < EC; c += 8)
-            dst[(c0 + c) / 8] = make_uint4(ptx::pack_bf16x2(z ? 0.f : a[c] * f, z ? 0.f : a[c + 1] * f),
-                                           ptx::pack_bf16x2(z ? 0.f : a[c + 2] * f, z ? 0.f : a[c + 3] * f),
-                                           ptx::pack_bf16x2(z ? 0.f : a[c + 4] * f, z ? 0.f : a[c + 5] * f),
-                                           ptx::pack_bf16x2(z ? 0.f : a[c + 6] * f, z ? 0.f : a[c + 7] * f));
+            for (int c = 0; c < EC; c += 8) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = z ? 0.f : a[c + e] * f;
+              if (acc) {
+                const uint4 prev = dst[(c0 + c) / 8];
+                const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&prev);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 pf = __bfloat1622float2(p2[e]);
+                  o[2 * e] += pf.x;
+                  o[2 * e + 1] += pf.y;
+                }
+              }
+              dst[(c0 + c) / 8] = make_uint4(ptx::pack_bf16x2(o[0], o[1]), ptx::pack_bf16x2(o[2], o[3]),
+                                             ptx::pack_bf16x2(o[4], o[5]), ptx::pack_bf16x2(o[6], o[7]));
+            }
+          }
         }
-      }
+      };
+      if (hf) write_row(std::integral_constant<int, D>{}, kColDK, p.dk, n_tiles > 0 ? p.scale : 1.0f, false);
+      else write_row(std::integral_constant<int, DV>{}, kColDV, p.dv, p.dout_scale, p.dv_accumulate != 0);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -709,16 +753,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// D_i = sum_c dO_ic O_ic, L2_i = LSE_i log2(e) (a row that saw no key:
-// +inf, so that its P is 0), and the dQ accumulator zeroed; D / 8 lanes per
-// row, 16 bytes of O and dO each.
-template <int D>
+// D_i = dout_scale * sum_c dO_ic O_ic, L2_i = LSE_i log2(e) (a row that saw
+// no key: +inf, so that its P is 0), and the dQ accumulator zeroed; DV / 8
+// lanes per row, 16 bytes of O and dO each, D / (DV / 8) accumulator values.
+template <int D, int DV>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
-  constexpr int LPR = D / 8;
+  constexpr int LPR = DV / 8;
+  constexpr int ZPL = D / LPR;  // accumulator floats zeroed per lane (4 or 8)
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (256 / LPR) + threadIdx.x / LPR;
   const int sub = threadIdx.x % LPR;
   const bool valid = row < p.rows;
-  const int64_t off = (valid ? row : 0) * D + sub * 8;
+  const int64_t off = (valid ? row : 0) * DV + sub * 8;
   const uint4 ov = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.out) + off));
   const uint4 gv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off));
   const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -732,11 +777,11 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant
 #pragma unroll
   for (int w = LPR / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
   if (!valid) return;
-  float4* acc = reinterpret_cast<float4*>(p.dq_acc + off);
-  acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4* acc = reinterpret_cast<float4*>(p.dq_acc + row * D + sub * ZPL);
+#pragma unroll
+  for (int i = 0; i < ZPL / 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (sub == 0) {
-    p.dvec[row] = s;
+    p.dvec[row] = s * p.dout_scale;
     const float l = p.lse[row];
     p.l2[row] = l == -CUDART_INF_F ? CUDART_INF_F : l * kLog2e;
   }
@@ -755,10 +800,10 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const __grid_constan
                  ptx::pack_bf16x2(c.x * f, c.y * f), ptx::pack_bf16x2(c.z * f, c.w * f));
 }
 
-template <int D, int SCORE>
+template <int D, int DV, int SCORE>
 cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
-  auto kern = attn_bwd_kernel<D, SCORE>;
-  constexpr int smem = BwdLayout<D>::SMEM;
+  auto kern = attn_bwd_kernel<D, DV, SCORE>;
+  constexpr int smem = BwdLayout<D, DV>::SMEM;
   static const cudaError_t checked = [&]() {
     cudaFuncAttributes a{};
     cudaError_t e = cudaFuncGetAttributes(&a, kern);
@@ -767,8 +812,8 @@ cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStrea
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   }();
   if (checked != cudaSuccess) return checked;
-  const int rgrid = static_cast<int>((p.rows + 256 / (D / 8) - 1) / (256 / (D / 8)));
-  attn_bwd_pre_kernel<D><<<rgrid, 256, 0, s>>>(p);
+  const int rgrid = static_cast<int>((p.rows + 256 / (DV / 8) - 1) / (256 / (DV / 8)));
+  attn_bwd_pre_kernel<D, DV><<<rgrid, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kern<<<p.B * p.Hkv * p.n_ktiles, kBwdThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
@@ -779,22 +824,23 @@ cudaError_t launch_bwd_ds(const CUtensorMap* maps, const BwdParams& p, cudaStrea
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_bwd_d(int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
   switch (score_mod) {
-    case SCORE_NONE: return launch_bwd_ds<D, SCORE_NONE>(maps, p, s);
-    case SCORE_ALIBI: return launch_bwd_ds<D, SCORE_ALIBI>(maps, p, s);
-    default: return launch_bwd_ds<D, SCORE_SOFTCAP>(maps, p, s);
+    case SCORE_NONE: return launch_bwd_ds<D, DV, SCORE_NONE>(maps, p, s);
+    case SCORE_ALIBI: return launch_bwd_ds<D, DV, SCORE_ALIBI>(maps, p, s);
+    default: return launch_bwd_ds<D, DV, SCORE_SOFTCAP>(maps, p, s);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(int d, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+cudaError_t launch_bwd(int d, int dv, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s) {
+  if (dv != d) return launch_bwd_d<64, 128>(score_mod, maps, p, s);
   switch (d) {
-    case 32: return launch_bwd_d<32>(score_mod, maps, p, s);
-    case 64: return launch_bwd_d<64>(score_mod, maps, p, s);
-    default: return launch_bwd_d<128>(score_mod, maps, p, s);
+    case 32: return launch_bwd_d<32, 32>(score_mod, maps, p, s);
+    case 64: return launch_bwd_d<64, 64>(score_mod, maps, p, s);
+    default: return launch_bwd_d<128, 128>(score_mod, maps, p, s);
   }
 }
 

@@ -10,12 +10,12 @@
 namespace fl {
 
 struct BwdParams {
-  const void* out;        // bf16 [B, Hq, Lq, D] forward output
-  const void* dout;       // bf16 [B, Hq, Lq, D] gradient of the output
+  const void* out;        // bf16 [B, Hq, Lq, DV] forward output
+  const void* dout;       // bf16 [B, Hq, Lq, DV] gradient of the output
   const float* lse;       // fp32 [B, Hq, Lq] forward log-sum-exp (natural log)
   void* dq;               // bf16 [B, Hq, Lq, D]
   void* dk;               // bf16 [B, Hkv, Lk, D]
-  void* dv;               // bf16 [B, Hkv, Lk, D]
+  void* dv;               // bf16 [B, Hkv, Lk, DV]
   float* dq_acc;          // fp32 [B, Hq, Lq, D] workspace
   float* dvec;            // fp32 [B, Hq, Lq] workspace: rowsum(dO * O)
   float* l2;              // fp32 [B, Hq, Lq] workspace: LSE * log2(e)
@@ -32,8 +32,14 @@ struct BwdParams {
   float sc_q[4];
   float sc_smax;
   int mask_kind, doc_causal, window, prefix, num_docs;
+  // the gradients are those of dout_scale * dout (1 for the plain backward;
+  // -lambda for the second branch of differential attention), and with
+  // dv_accumulate the kernel adds its dV to the bf16 values already in dv
+  float dout_scale;
+  int dv_accumulate;
 };
 
-cudaError_t launch_bwd(int d, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
+// (d, dv): (32, 32), (64, 64), (128, 128) or (64, 128)
+cudaError_t launch_bwd(int d, int dv, int score_mod, const CUtensorMap* maps, const BwdParams& p, cudaStream_t s);
 
 }  // namespace fl

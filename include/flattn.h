@@ -241,8 +241,9 @@ FL_API size_t fl_attn_decode_workspace_size(const fl_attn_desc* desc);
  *   workspace        : caller-owned device buffer of at least
  *                      fl_attn_bwd_workspace_size(desc) bytes (16-byte
  *                      aligned): an fp32 dq accumulator and two per-row vectors
- * desc: the forward's descriptor; d == dv in {32, 64, 128}, Lq a multiple of 4,
- * strides zero.  Masks, ALiBi and softcap as in fl_attn_fwd.
+ * desc: the forward's descriptor; d == dv in {32, 64, 128}, or d 64 with
+ * dv 128 (v, dv: [B, Hkv, Lk, dv]; out, dout: [B, Hq, Lq, dv]); Lq a
+ * multiple of 4, strides zero.  Masks, ALiBi and softcap as in fl_attn_fwd.
  */
 FL_API fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                              const float* lse, void* dq, void* dk, void* dv, void* workspace,
@@ -250,6 +251,32 @@ FL_API fl_status fl_attn_bwd(const void* q, const void* k, const void* v, const 
 
 /* Workspace bytes fl_attn_bwd needs for `desc` (0 on an invalid descriptor). */
 FL_API size_t fl_attn_bwd_workspace_size(const fl_attn_desc* desc);
+
+/*
+ * Backward of fl_diffattn_fwd (differential attention, Flashlight technical
+ * summary, Results: differential attention among the variants; the training
+ * backward is future work in the wiki summary, 局限与 Future Work).  With
+ * out = O1 - lambda O2, O_i = softmax(scale Q_i K_i^T [+ causal mask]) V, and
+ * dout = dL/dout, returns the plain derivatives
+ *   dq_i, dk_i : those of attention branch i for the output gradient dout
+ *                (i = 1) or -lambda dout (i = 2)
+ *   dv         : the sum of both branches' dV
+ *   q1, k1, q2, k2, dq1, dk1, dq2, dk2 : bf16 [B, H, L, 64] contiguous
+ *   v, dout, dv                        : bf16 [B, H, L, 128] contiguous
+ *   workspace : caller-owned device buffer of at least
+ *               fl_diffattn_bwd_workspace_size(desc) bytes (16-byte aligned);
+ *               the call recomputes O1, O2 and their LSEs into it (the fused
+ *               forward keeps only O1 - lambda O2)
+ * desc: as for fl_diffattn_fwd (Hkv == Hq, Lk == Lq, d 64, dv 128, mask NONE
+ * or CAUSAL, no score_mod, strides zero), and Lq a multiple of 4.  Errors as
+ * fl_attn_bwd; asynchronous on desc->stream.
+ */
+FL_API fl_status fl_diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                                 const void* dout, float lambda, void* dq1, void* dk1, void* dq2, void* dk2,
+                                 void* dv, void* workspace, size_t workspace_bytes, const fl_attn_desc* desc);
+
+/* Workspace bytes fl_diffattn_bwd needs for `desc` (0 on an invalid descriptor). */
+FL_API size_t fl_diffattn_bwd_workspace_size(const fl_attn_desc* desc);
 
 /*
  * Allocation-free variant of fl_attn_fwd (no counterpart in the paper; it is

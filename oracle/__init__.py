@@ -12,7 +12,7 @@ brute-force loops that pin each one).
 """
 from .attention import *  # noqa: F401,F403
 from .attention import __all__ as _att_all
-from .backward import attention_backward  # noqa: F401
+from .backward import attention_backward, diff_attention_backward  # noqa: F401
 from .online import online_attention  # noqa: F401
 
-__all__ = list(_att_all) + ["online_attention", "attention_backward"]
+__all__ = list(_att_all) + ["online_attention", "attention_backward", "diff_attention_backward"]

@@ -25,7 +25,7 @@ import numpy as np
 
 from .attention import _f64, apply_score_mod, softmax_rows, visibility
 
-__all__ = ["attention_backward"]
+__all__ = ["attention_backward", "diff_attention_backward"]
 
 
 def attention_backward(q, k, v, dout, *, scale: float | None = None, mask: str = "none",
@@ -63,3 +63,18 @@ def attention_backward(q, k, v, dout, *, scale: float | None = None, mask: str =
             dq[b, h] += scale * (dT @ k[b, g])
             dk[b, g] += scale * (dT.T @ q[b, h])
     return dq, dk, dv
+
+
+def diff_attention_backward(q1, k1, q2, k2, v, dout, lam: float, *, scale: float | None = None,
+                            causal: bool = True):
+    """(dq1, dk1, dq2, dk2, dv) of L = sum(dout * diff_attention(...)) in
+    float64.  The output O1 - lam * O2 is linear in the two branch outputs,
+    so branch 1 takes the output gradient dout and branch 2 takes -lam * dout.
+    Both branches read the same V, so dv is the sum of the two branch dV's."""
+    d = _f64(q1).shape[-1]
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    mask = "causal" if causal else "none"
+    dout = _f64(dout)
+    dq1, dk1, dv1 = attention_backward(q1, k1, v, dout, scale=scale, mask=mask)
+    dq2, dk2, dv2 = attention_backward(q2, k2, v, -float(lam) * dout, scale=scale, mask=mask)
+    return dq1, dk1, dq2, dk2, dv1 + dv2

@@ -156,8 +156,8 @@ def test_decode_rejects(L):
 
 def test_bwd_rejects(L):
     """fl_attn_bwd's argument checks, all of which return before any CUDA
-    call; d = dv = 128 passes the dimension check and is stopped here only by
-    the workspace size."""
+    call; d = dv in {32, 64, 128} and (d, dv) = (64, 128) pass the dimension
+    check and are stopped here only by the workspace size."""
     f = L.fl_attn_bwd
     ws = L.fl_attn_bwd_workspace_size
 
@@ -169,7 +169,7 @@ def test_bwd_rejects(L):
 
     assert f(P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t(1 << 30), None) == _lib.FL_ERR_INVALID_ARG
     assert call(_desc(), lse=0) == _lib.FL_ERR_INVALID_ARG
-    for d, dv in ((96, 96), (64, 128), (128, 64), (256, 256), (16, 16)):
+    for d, dv in ((96, 96), (32, 64), (128, 64), (64, 32), (256, 256), (16, 16)):
         assert call(_desc(d=d, dv=dv)) == _lib.FL_ERR_UNSUPPORTED, (d, dv)
     assert call(_desc(mask_kind=1, Lk=256)) == _lib.FL_ERR_UNSUPPORTED      # masked Lq != Lk
     assert call(_desc(Lq=130, Lk=130)) == _lib.FL_ERR_UNSUPPORTED           # Lq % 4
@@ -177,12 +177,48 @@ def test_bwd_rejects(L):
     assert call(_desc(score_mod=1)) == _lib.FL_ERR_INVALID_ARG              # ALiBi without slopes
     assert call(_desc(), dk=P + 8) == _lib.FL_ERR_ALIGNMENT
     assert call(_desc(), lse=P + 2) == _lib.FL_ERR_ALIGNMENT
-    for d in (32, 64, 128):
-        desc = _desc(d=d, dv=d)
+    for d, dv in ((32, 32), (64, 64), (128, 128), (64, 128)):
+        desc = _desc(d=d, dv=dv)
         need = ws(ctypes.byref(desc))
         assert need == 1 * 2 * 128 * (d + 2) * 4
         assert call(desc, nbytes=need - 1) == _lib.FL_ERR_INVALID_ARG, d
         assert call(desc, workspace=0) == _lib.FL_ERR_INVALID_ARG, d
+
+
+def test_diffattn_bwd_rejects(L):
+    """fl_diffattn_bwd's argument checks (none reaches CUDA)."""
+    f = L.fl_diffattn_bwd
+    ws = L.fl_diffattn_bwd_workspace_size
+
+    def dd(**kw):
+        base = dict(B=1, Hq=2, Hkv=2, Lq=256, Lk=256, d=64, dv=128, mask_kind=1)
+        base.update(kw)
+        return _desc(**base)
+
+    def call(desc, lam=0.8, nbytes=None, **over):
+        a = dict(q1=P, k1=P, q2=P, k2=P, v=P, dout=P)
+        o = dict(dq1=P, dk1=P, dq2=P, dk2=P, dv=P, workspace=P)
+        a.update({k: v for k, v in over.items() if k in a})
+        o.update({k: v for k, v in over.items() if k in o})
+        n = ws(ctypes.byref(desc)) if nbytes is None else nbytes
+        return f(*a.values(), ctypes.c_float(lam), *o.values(), ctypes.c_size_t(n), ctypes.byref(desc))
+
+    rows = 1 * 2 * 256
+    assert ws(ctypes.byref(dd())) == rows * (2 * 128 * 2 + 66 * 4 + 8)
+    assert f(P, P, P, P, P, P, ctypes.c_float(0.8), P, P, P, P, P, P, ctypes.c_size_t(1 << 30), None) == \
+        _lib.FL_ERR_INVALID_ARG
+    assert call(dd(), dq2=0) == _lib.FL_ERR_INVALID_ARG
+    assert call(dd(), lam=float("nan")) == _lib.FL_ERR_INVALID_ARG
+    assert call(dd(Hkv=1)) == _lib.FL_ERR_INVALID_ARG
+    assert call(dd(Lk=128)) == _lib.FL_ERR_INVALID_ARG
+    assert call(dd(d=32, dv=128)) == _lib.FL_ERR_UNSUPPORTED
+    assert call(dd(dv=64)) == _lib.FL_ERR_UNSUPPORTED
+    assert call(dd(mask_kind=2, window=8)) == _lib.FL_ERR_UNSUPPORTED
+    assert call(dd(score_mod=2, softcap=30.0)) == _lib.FL_ERR_UNSUPPORTED
+    assert call(dd(Lq=258, Lk=258)) == _lib.FL_ERR_UNSUPPORTED
+    assert call(dd(), dv=P + 8) == _lib.FL_ERR_ALIGNMENT
+    assert call(dd(), workspace=P + 4) == _lib.FL_ERR_ALIGNMENT
+    assert call(dd(), nbytes=ws(ctypes.byref(dd())) - 1) == _lib.FL_ERR_INVALID_ARG
 
 
 def test_decode_split_arithmetic():

@@ -143,3 +143,80 @@ def test_bwd_d128_fullsize_sampled_heads(kw):
         _cmp(dq[sl], rq, f"dq[{b},{h}]")
         _cmp(dk[sl], rk, f"dk[{b},{h}]")
         _cmp(dv[sl], rv, f"dv[{b},{h}]")
+
+
+# value head dim 128 with query/key head dim 64 (the differential attention
+# branches' shape): own TMEM map (dV 128 columns, dK and dQ 64 each)
+DV_CASES = [
+    (1, 2, 2, 256, dict()),
+    (1, 2, 2, 300, dict(mask="causal")),
+    (2, 8, 2, 300, dict(mask="causal")),
+    (1, 4, 4, 300, dict(score_mod="alibi", mask="causal")),
+    (1, 2, 2, 300, dict(score_mod="softcap", softcap=5.0)),
+    (1, 2, 2, 520, dict(mask="window", window=100)),
+    (2, 4, 4, 1024, dict(mask="causal")),
+]
+
+
+@pytest.mark.parametrize("case", DV_CASES, ids=lambda c: f"B{c[0]}H{c[1]}x{c[2]}L{c[3]}-" +
+                         "-".join(f"{k}{v}" for k, v in c[4].items()))
+def test_bwd_value_head_dim_128(case):
+    B, Hq, Hkv, L, kw = case
+    q, k, v = synth.attn_inputs(B, Hq, Hkv, L, 64, dv=128, seed=L + 5)
+    dout = synth.randn_bf16((B, Hq, L, 128), synth.generator(L + 9))
+    gkw, okw = dict(kw), dict(kw)
+    if kw.get("score_mod") == "alibi":
+        s = synth.alibi_slopes(Hq)
+        gkw["alibi_slopes"], okw["slopes"] = s.to(DEV), s
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    out, lse = attn_fwd(qd, kd, vd, **gkw)
+    dq, dk, dv = attn_bwd(qd, kd, vd, out, dod, lse, **gkw)
+    sync_status()
+    assert dv.shape == v.shape
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, **okw)
+    _cmp(dq, rq, "dq")
+    _cmp(dk, rk, "dk")
+    _cmp(dv, rv, "dv")
+
+
+DIFF_CASES = [
+    # (B, H, L, causal, lambda)
+    (1, 2, 256, True, 0.8),
+    (1, 2, 300, False, 0.5),
+    (2, 4, 520, True, 0.8),
+    (1, 2, 260, True, 0.0),
+    (1, 2, 384, True, -1.5),
+]
+
+
+@pytest.mark.parametrize("case", DIFF_CASES, ids=lambda c: f"B{c[0]}H{c[1]}L{c[2]}causal{c[3]}lam{c[4]}")
+def test_diffattn_bwd_parity(case):
+    from flashattention_attn_fwd_gb300 import diffattn_bwd
+    B, H, L, causal, lam = case
+    q1, k1, q2, k2, v = synth.diff_inputs(B, H, L, seed=L + 21)
+    dout = synth.randn_bf16((B, H, L, 128), synth.generator(L + 23))
+    dq1, dk1, dq2, dk2, dv = diffattn_bwd(*(t.to(DEV) for t in (q1, k1, q2, k2, v, dout)), lam, causal=causal)
+    sync_status()
+    ref = oracle.diff_attention_backward(q1, k1, q2, k2, v, dout, lam, causal=causal)
+    for name, g, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), (dq1, dk1, dq2, dk2, dv), ref):
+        if lam == 0.0 and name in ("dq2", "dk2"):
+            assert float(g.abs().max()) == 0.0, name
+            continue
+        _cmp(g, r, name)
+
+
+# The differential forward's workload (B 4, H 16, L 4096, causal, lambda
+# 0.8): all five gradients of two sampled heads against the oracle (heads
+# are independent).
+def test_diffattn_bwd_fullsize_sampled_heads():
+    from flashattention_attn_fwd_gb300 import diffattn_bwd
+    B, H, L, lam = 4, 16, 4096, 0.8
+    q1, k1, q2, k2, v = synth.diff_inputs(B, H, L, seed=40)
+    dout = synth.randn_bf16((B, H, L, 128), synth.generator(41))
+    grads = diffattn_bwd(*(t.to(DEV) for t in (q1, k1, q2, k2, v, dout)), lam, causal=True)
+    sync_status()
+    for b, h in ((0, 3), (3, 14)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.diff_attention_backward(q1[sl], k1[sl], q2[sl], k2[sl], v[sl], dout[sl], lam, causal=True)
+        for name, g, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), grads, ref):
+            _cmp(g[sl], r, f"{name}[{b},{h}]")

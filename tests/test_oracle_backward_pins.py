@@ -119,3 +119,43 @@ def test_backward_gqa_sums_group_gradients():
     np.testing.assert_allclose(dq, dq2, atol=1e-12)
     np.testing.assert_allclose(dk, dk2.reshape(B, Hkv, grp, L, d).sum(2), atol=1e-12)
     np.testing.assert_allclose(dv, dv2.reshape(B, Hkv, grp, L, d).sum(2), atol=1e-12)
+
+
+# Differential attention backward: central finite differences of
+# L = sum(dO * out) through the separately pinned forward oracle
+# (oracle.diff_attention), for every one of the five inputs, causal and not;
+# a dropped branch, a wrong sign of lambda or a missing dV term fails it.
+@pytest.mark.parametrize("causal", [True, False])
+def test_diff_backward_finite_differences(causal):
+    B, H, L, d, dv, lam = 1, 2, 5, 3, 4, 0.6
+    q1, k1, q2, k2 = (_rand(B, H, L, d) for _ in range(4))
+    v, dout = _rand(B, H, L, dv), _rand(B, H, L, dv)
+    grads = oracle.diff_attention_backward(q1, k1, q2, k2, v, dout, lam, causal=causal)
+    eps = 1e-6
+
+    def loss(*a):
+        o, _, _ = oracle.diff_attention(*a, lam, causal=causal)
+        return float(np.sum(o * dout))
+
+    base = [q1, k1, q2, k2, v]
+    for which in range(5):
+        for idx in [(0, 0, 0, 0), (0, 1, 4, 2), (0, 1, 2, 1), (0, 0, 3, 0)]:
+            p, m = [a.copy() for a in base], [a.copy() for a in base]
+            p[which][idx] += eps
+            m[which][idx] -= eps
+            fd = (loss(*p) - loss(*m)) / (2 * eps)
+            assert grads[which][idx] == pytest.approx(fd, abs=1e-7), (which, idx)
+
+
+def test_diff_backward_lambda_zero_is_branch_one():
+    """lambda = 0: the second branch gets no gradient and the rest is the
+    plain attention backward of branch 1."""
+    B, H, L, d, dv = 1, 2, 7, 4, 6
+    q1, k1, q2, k2 = (_rand(B, H, L, d) for _ in range(4))
+    v, dout = _rand(B, H, L, dv), _rand(B, H, L, dv)
+    dq1, dk1, dq2, dk2, dvv = oracle.diff_attention_backward(q1, k1, q2, k2, v, dout, 0.0, causal=True)
+    rq, rk, rv = oracle.attention_backward(q1, k1, v, dout, mask="causal")
+    assert np.array_equal(dq2, np.zeros_like(dq2)) and np.array_equal(dk2, np.zeros_like(dk2))
+    np.testing.assert_allclose(dq1, rq, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk1, rk, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dvv, rv, rtol=0, atol=1e-13)
