@@ -161,7 +161,8 @@ def make_calls(api, bufs, slopes):
 # another family uses, so a change to (say) the backward leaves the forward
 # kernels' counters valid.
 KERNEL_FAMILY_EXCLUDES = {"forward": ("bwd.", "decode."), "backward": ("decode.",), "decode": ("bwd.",)}
-TRAFFIC_FAMILY = {"decode": "decode", "backward": "backward", "backward_d128": "backward"}  # else forward
+TRAFFIC_FAMILY = {"decode": "decode", "backward": "backward", "backward_d128": "backward",
+                  "diffattn_backward": "backward"}  # every other entry: forward
 
 
 def kernel_source_hash(family="forward"):
@@ -286,6 +287,20 @@ def variant_configs():
             return call, tf, ef, by, f"1 input set ({mb:.0f} MB of inputs, outputs and dq accumulator)"
         return name, build
 
+    def diff_bwd():
+        def build():
+            q1, k1, q2, k2, v = (t.to(dev) for t in synth.diff_inputs(4, 16, 4096, seed=40))
+            dout = synth.randn_bf16((4, 16, 4096, 128), synth.generator(41)).to(dev)
+            grads = [torch.empty_like(t) for t in (q1, k1, q2, k2, v)]
+            ws = torch.empty(4 * 16 * 4096 * 784, device=dev, dtype=torch.uint8)
+            tf, ef, by = F.diff_bwd_counts(4, 16, 4096)
+
+            def call():
+                api.diffattn_bwd(q1, k1, q2, k2, v, dout, 0.8, causal=True, dq1=grads[0], dk1=grads[1],
+                                 dq2=grads[2], dk2=grads[3], dv=grads[4], workspace=ws)
+            return call, tf, ef, by, "1 input set (268 MB of inputs, 201 MB of gradients, 206 MB workspace)"
+        return "4b diffattn backward B4 H16 L4096 causal lambda0.8", build
+
     def evo():
         def build():
             sets = []
@@ -310,6 +325,7 @@ def variant_configs():
         attn("3a gqa32/8 doc8 B2 L8192 d64", 2, 32, 8, 8192, 64, 2, 11, mask="document"),
         attn("3b gqa32/8 prefix1024 B2 L8192 d64", 2, 32, 8, 8192, 64, 2, 13, mask="prefix_lm", prefix=1024),
         diff(),
+        diff_bwd(),
         evo(),
         evo_col(),
         decode(),

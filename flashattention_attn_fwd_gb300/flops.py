@@ -84,6 +84,19 @@ def bwd_counts(B, Hq, Hkv, L, d, *, mask="none", window=None, prefix=None, doc_o
     return int(tf * f), int(ef * f), bytes_
 
 
+def diff_bwd_counts(B, H, L, d=64, dv=128, causal=True):
+    """Backward of differential attention as fl_diffattn_bwd runs it: per
+    branch the forward recomputed (2 d + 2 dv FLOPs per visible pair) and the
+    five backward products (S and dP recomputed, dV, dK, dQ: 2 (3 d + 2 dv));
+    bytes read q1, k1, q2, k2, v, dout and written their five gradients once."""
+    tf, ef, _ = attn_counts(B, H, H, L, d, dv, mask="causal" if causal else "none")
+    per_fwd = 2 * d + 2 * dv
+    per_all = 2 * (per_fwd + 2 * (3 * d + 2 * dv))
+    n = B * H * L
+    bytes_ = 2 * (4 * n * d + 2 * n * dv) + 2 * (4 * n * d + n * dv)
+    return tf // per_fwd * per_all, ef // per_fwd * per_all, bytes_
+
+
 def diff_counts(B, H, L, d=64, dv=128, causal=True):
     lo, hi = row_intervals("causal" if causal else "none", L)
     tiles, pairs = visible_tiles(lo, hi, L), visible_pairs(lo, hi)
