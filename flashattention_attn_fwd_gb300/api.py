@@ -320,6 +320,27 @@ def attention(q, k, v, **kw):
     return _Attention.apply(q, k, v, kw)
 
 
+class _DiffAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q1, k1, q2, k2, v, lam, causal, scale):
+        out, _ = diffattn_fwd(q1, k1, q2, k2, v, lam, causal=causal, scale=scale, return_lse=False)
+        ctx.save_for_backward(q1, k1, q2, k2, v)
+        ctx.args = (lam, causal, scale)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        lam, causal, scale = ctx.args
+        grads = diffattn_bwd(*ctx.saved_tensors, dout.contiguous(), lam, causal=causal, scale=scale)
+        return (*grads, None, None, None)
+
+
+def diff_attention(q1, k1, q2, k2, v, lam: float, *, causal: bool = True, scale: float | None = None):
+    """Differentiable differential attention: diffattn_fwd in the forward,
+    diffattn_bwd (gradients of q1, k1, q2, k2 and v) in the backward."""
+    return _DiffAttention.apply(q1, k1, q2, k2, v, float(lam), causal, scale)
+
+
 def sync_status(stream=None) -> int:
     """fl_sync_status: synchronise the stream and return (and clear) the
     device status word; raises FlattnError if a kernel reported a failure."""

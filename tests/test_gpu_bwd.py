@@ -220,3 +220,17 @@ def test_diffattn_bwd_fullsize_sampled_heads():
         ref = oracle.diff_attention_backward(q1[sl], k1[sl], q2[sl], k2[sl], v[sl], dout[sl], lam, causal=True)
         for name, g, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), grads, ref):
             _cmp(g[sl], r, f"{name}[{b},{h}]")
+
+
+def test_diff_attention_autograd_matches_oracle():
+    from flashattention_attn_fwd_gb300 import diff_attention
+    B, H, L, lam = 1, 2, 256, 0.8
+    q1, k1, q2, k2, v = synth.diff_inputs(B, H, L, seed=12)
+    dout = synth.randn_bf16((B, H, L, 128), synth.generator(13))
+    ins = [t.to(DEV).requires_grad_() for t in (q1, k1, q2, k2, v)]
+    out = diff_attention(*ins, lam, causal=True)
+    out.backward(dout.to(DEV))
+    sync_status()
+    ref = oracle.diff_attention_backward(q1, k1, q2, k2, v, dout, lam, causal=True)
+    for name, t, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), ins, ref):
+        _cmp(t.grad, r, name)
