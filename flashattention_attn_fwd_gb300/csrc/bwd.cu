@@ -30,7 +30,12 @@
 // columns (dP^T of the next tile waits until the dQ warps have read dQ),
 // sech^2 goes over the second half of each half-tile's S^T columns, and K, V
 // stay in shared memory, as does one dO buffer (two do not fit beside the
-// rest).
+// rest).  With d = 64 and dv = 128 (the branches of differential
+// attention) dP^T is at [128,256), dV [256,384), dK [384,448), dQ
+// [448,512), sech^2 as at d = 128.  The gradients may be those of a scaled
+// output gradient (dout_scale, applied to dP, D and dV), and dV may be added
+// to what dv holds: the differential backward's second branch takes
+// -lambda dout and adds its dV to the first branch's.
 // Warp roles (512 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 4-11
 // compute P and dS (one thread per key row and half of the query columns:
 // two warps per scheduler), warps 12-15 add dQ into the accumulator (one
